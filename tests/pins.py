@@ -1,0 +1,313 @@
+"""Pins of the fp64 oracle to facts it does not compute itself.
+
+Each ``pin_*`` takes an ``oracle.Oracle`` and raises ``AssertionError`` when
+the oracle disagrees with:
+  * exact rational brute force (``fractions.Fraction``, ``decimal`` at 60
+    digits) on tiny inputs,
+  * integer-exact cases, closed forms and invariants of the definitions,
+  * independent library routines (numpy float64 matmul, torch CPU float64
+    scaled_dot_product_attention / rms_norm / silu).
+The shapes are non-square and the data non-symmetric so that a transposed
+operand, a wrong index or sign, or a dropped term fails at least one pin;
+``test_oracle_mutations.py`` plants such mistakes in a copy of the oracle and
+checks that they are caught.
+"""
+from __future__ import annotations
+
+import math
+from decimal import Decimal, getcontext
+from fractions import Fraction
+
+import numpy as np
+import torch
+import torch.nn.functional as F
+
+U64 = 2.0 ** -53  # unit roundoff of fp64
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _fp32_vals(rng, shape, scale=1.0):
+    """Random values exactly representable in fp32 (so Fraction(x) is the stored value)."""
+    return (rng.standard_normal(shape) * scale).astype(np.float32).astype(np.float64)
+
+
+def _close(got, want, bound, what):
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    err = np.abs(got - want)
+    bad = ~(err <= bound)
+    assert not bad.any(), "%s: max err %.3e, bound %.3e at %s" % (
+        what, float(err.max()), float(np.max(bound)), np.argwhere(bad)[0])
+
+
+# ------------------------------------------------------------------ GEMM pins
+
+GEMM_SHAPES = [(1, 1, 1), (2, 3, 4), (3, 2, 5), (4, 5, 3), (3, 4, 4)]
+
+
+def pin_linear_bruteforce(O):
+    """linear == exact rational sum, within (K+1)*u*nrm; nrm == exact sum of |terms|."""
+    rng = _rng(1)
+    for (M, N, K) in GEMM_SHAPES:
+        for with_bias in (False, True):
+            x = _fp32_vals(rng, (M, K)); w = _fp32_vals(rng, (N, K))
+            bias = _fp32_vals(rng, (N,)) if with_bias else None
+            y, nrm = O.linear(x, w, bias)
+            for m in range(M):
+                for n in range(N):
+                    terms = [Fraction(x[m, k]) * Fraction(w[n, k]) for k in range(K)]
+                    if with_bias:
+                        terms.append(Fraction(bias[n]))
+                    exact = sum(terms, Fraction(0))
+                    mag = sum((abs(t) for t in terms), Fraction(0))
+                    tol = (K + 2) * U64 * float(mag)
+                    assert abs(Fraction(y[m, n]) - exact) <= Fraction(tol), \
+                        "linear(%d,%d,%d)[%d,%d]" % (M, N, K, m, n)
+                    assert abs(Fraction(nrm[m, n]) - mag) <= Fraction(tol), "linear nrm"
+
+
+def pin_matmul_bruteforce(O):
+    rng = _rng(2)
+    for (M, N, K) in GEMM_SHAPES:
+        a = _fp32_vals(rng, (M, K)); b = _fp32_vals(rng, (K, N))
+        y, nrm = O.matmul(a, b)
+        for m in range(M):
+            for n in range(N):
+                terms = [Fraction(a[m, k]) * Fraction(b[k, n]) for k in range(K)]
+                exact = sum(terms, Fraction(0))
+                mag = sum((abs(t) for t in terms), Fraction(0))
+                tol = (K + 1) * U64 * float(mag)
+                assert abs(Fraction(y[m, n]) - exact) <= Fraction(tol), \
+                    "matmul(%d,%d,%d)[%d,%d]" % (M, N, K, m, n)
+                assert abs(Fraction(nrm[m, n]) - mag) <= Fraction(tol), "matmul nrm"
+
+
+def pin_addmm_bruteforce(O):
+    rng = _rng(3)
+    for (M, N, K) in GEMM_SHAPES:
+        for (alpha, beta) in ((1.0, 1.0), (0.5, -2.0), (0.0, 1.0), (1.0, 0.0), (-1.5, 0.25)):
+            for c_row in (False, True):
+                a = _fp32_vals(rng, (M, K)); b = _fp32_vals(rng, (K, N))
+                c = _fp32_vals(rng, (N,) if c_row else (M, N))
+                y, nrm = O.addmm(c, a, b, alpha, beta)
+                for m in range(M):
+                    for n in range(N):
+                        s = sum((Fraction(a[m, k]) * Fraction(b[k, n]) for k in range(K)),
+                                Fraction(0))
+                        mag = sum((abs(Fraction(a[m, k]) * Fraction(b[k, n])) for k in range(K)),
+                                  Fraction(0))
+                        cv = Fraction(c[n] if c_row else c[m, n])
+                        exact = Fraction(beta) * cv + Fraction(alpha) * s
+                        emag = abs(Fraction(alpha)) * mag + abs(Fraction(beta) * cv)
+                        tol = (K + 3) * U64 * float(emag)
+                        assert abs(Fraction(y[m, n]) - exact) <= Fraction(tol), \
+                            "addmm a=%g b=%g row=%d (%d,%d,%d)[%d,%d]" % (
+                                alpha, beta, c_row, M, N, K, m, n)
+                        assert abs(Fraction(nrm[m, n]) - emag) <= Fraction(tol), "addmm nrm"
+
+
+def pin_gemm_integer_exact(O):
+    """Small integers: every partial sum is exact in fp64, so the result is the integer product."""
+    rng = _rng(4)
+    M, N, K = 7, 9, 33
+    a = rng.integers(-2, 3, (M, K)).astype(np.float64)
+    b = rng.integers(-2, 3, (K, N)).astype(np.float64)
+    bias = rng.integers(-3, 4, (N,)).astype(np.float64)
+    want = (a.astype(np.int64) @ b.astype(np.int64)).astype(np.float64)
+    y, _ = O.matmul(a, b)
+    assert np.array_equal(y, want), "matmul integer-exact"
+    y, _ = O.linear(a, b.T.copy(), bias)
+    assert np.array_equal(y, want + bias), "linear integer-exact"
+    y, _ = O.addmm(bias, a, b, 3.0, -2.0)
+    assert np.array_equal(y, 3.0 * want - 2.0 * bias), "addmm integer-exact"
+
+
+def pin_gemm_numpy(O):
+    """numpy float64 matmul (BLAS, another summation order): equal within 2*K*u*nrm."""
+    rng = _rng(5)
+    M, N, K = 37, 53, 129
+    a = rng.standard_normal((M, K)); b = rng.standard_normal((K, N))
+    y, nrm = O.matmul(a, b)
+    _close(y, a @ b, 2 * K * U64 * nrm, "matmul vs numpy")
+    w = rng.standard_normal((N, K)); bias = rng.standard_normal(N)
+    y, nrm = O.linear(a, w, bias)
+    _close(y, a @ w.T + bias, 2 * (K + 1) * U64 * nrm, "linear vs numpy")
+    c = rng.standard_normal((M, N))
+    y, nrm = O.addmm(c, a, b, 0.75, -1.25)
+    _close(y, -1.25 * c + 0.75 * (a @ b), 2 * (K + 2) * U64 * nrm, "addmm vs numpy")
+
+
+def pin_gemm_identities(O):
+    """w = I gives y = x + bias exactly; linear(x, w) == matmul(x, w^T) bit for bit."""
+    rng = _rng(6)
+    M, K = 5, 8
+    x = rng.standard_normal((M, K)); bias = rng.standard_normal(K)
+    y, _ = O.linear(x, np.eye(K), bias)
+    assert np.array_equal(y, x + bias), "linear with identity weight"
+    w = rng.standard_normal((11, K))
+    y1, n1 = O.linear(x, w)
+    y2, n2 = O.matmul(x, w.T.copy())
+    assert np.array_equal(y1, y2) and np.array_equal(n1, n2), "linear == matmul(w^T)"
+
+
+# ------------------------------------------------------------------ attention pins
+
+def _decimal_sdpa(q, k, v, causal, q_offset, scale):
+    """Softmax attention in 60-digit decimal arithmetic, straight from the definition."""
+    getcontext().prec = 60
+    B, H, Lq, D = q.shape
+    Hkv, Lkv = k.shape[1], k.shape[2]
+    G = H // Hkv
+    out = np.zeros(q.shape)
+    mag = np.zeros(q.shape)
+    sc = Decimal(scale)
+    for b in range(B):
+        for h in range(H):
+            hk = h // G
+            for i in range(Lq):
+                last = q_offset + i if causal else Lkv - 1
+                vis = [j for j in range(Lkv) if j <= last]
+                s = [sc * sum(Decimal(q[b, h, i, d]) * Decimal(k[b, hk, j, d]) for d in range(D))
+                     for j in vis]
+                mx = max(s)
+                e = [(x - mx).exp() for x in s]
+                den = sum(e)
+                for d in range(D):
+                    out[b, h, i, d] = float(sum(e[t] * Decimal(v[b, hk, j, d])
+                                                for t, j in enumerate(vis)) / den)
+                    mag[b, h, i, d] = float(sum(e[t] * abs(Decimal(v[b, hk, j, d]))
+                                                for t, j in enumerate(vis)) / den)
+    return out, mag
+
+
+def pin_sdpa_bruteforce(O):
+    rng = _rng(7)
+    B, H, Hkv, Lq, Lkv, D = 2, 4, 2, 3, 5, 3
+    q = rng.standard_normal((B, H, Lq, D)); k = rng.standard_normal((B, Hkv, Lkv, D))
+    v = rng.standard_normal((B, Hkv, Lkv, D))
+    for causal, q_offset, scale in ((True, 2, None), (True, 0, None), (True, 1, 0.7),
+                                    (False, 2, None), (False, 0, 1.3)):
+        sc = 1.0 / math.sqrt(D) if scale is None else scale
+        o, nrm = O.sdpa(q, k, v, causal=causal, q_offset=q_offset, scale=scale)
+        want, wmag = _decimal_sdpa(q, k, v, causal, q_offset, sc)
+        _close(o, want, 1e-13 * wmag, "sdpa brute force c=%s off=%d" % (causal, q_offset))
+        _close(nrm, wmag, 1e-13 * wmag, "sdpa normaliser c=%s off=%d" % (causal, q_offset))
+
+
+def _torch_sdpa_f64(q, k, v, causal, q_offset, scale):
+    """torch CPU float64 attention with an explicit boolean mask and repeated K/V heads."""
+    q, k, v = (torch.from_numpy(np.asarray(t, dtype=np.float64)) for t in (q, k, v))
+    B, H, Lq, D = q.shape
+    Hkv, Lkv = k.shape[1], k.shape[2]
+    G = H // Hkv
+    k = k.repeat_interleave(G, dim=1); v = v.repeat_interleave(G, dim=1)
+    i = torch.arange(Lq)[:, None]; j = torch.arange(Lkv)[None, :]
+    mask = (j <= q_offset + i) if causal else torch.ones(Lq, Lkv, dtype=torch.bool)
+    return F.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=scale).numpy()
+
+
+def pin_sdpa_torch(O):
+    rng = _rng(8)
+    B, H, Hkv, Lq, Lkv, D = 2, 6, 2, 7, 23, 16
+    q = rng.standard_normal((B, H, Lq, D)); k = rng.standard_normal((B, Hkv, Lkv, D))
+    v = rng.standard_normal((B, Hkv, Lkv, D))
+    for causal, q_offset in ((True, Lkv - Lq), (True, 3), (False, 0)):
+        sc = 1.0 / math.sqrt(D)
+        o, nrm = O.sdpa(q, k, v, causal=causal, q_offset=q_offset)
+        want = _torch_sdpa_f64(q, k, v, causal, q_offset, sc)
+        _close(o, want, 1e-12 * nrm + 1e-300, "sdpa vs torch causal=%s off=%d" % (causal, q_offset))
+
+
+def pin_sdpa_closed_forms(O):
+    rng = _rng(9)
+    B, H, Hkv, Lq, Lkv, D = 1, 4, 2, 4, 9, 8
+    q = rng.standard_normal((B, H, Lq, D)); k = rng.standard_normal((B, Hkv, Lkv, D))
+    v = rng.standard_normal((B, Hkv, Lkv, D))
+    # one visible key: query 0 at position 0 sees only key 0 -> o = v_0 exactly
+    o, _ = O.sdpa(q, k, v, causal=True, q_offset=0)
+    for h in range(H):
+        assert np.array_equal(o[0, h, 0], v[0, h // 2, 0]), "single visible key"
+    # identical keys -> uniform weights -> mean of the visible values
+    kc = np.broadcast_to(k[:, :, :1], k.shape).copy()
+    o, _ = O.sdpa(q, kc, v, causal=True, q_offset=3)
+    for h in range(H):
+        for i in range(Lq):
+            want = v[0, h // 2, :3 + i + 1].mean(axis=0)
+            _close(o[0, h, i], want, 1e-14 * np.abs(v[0, h // 2]).max(), "identical keys")
+    # constant values -> the constant; ones -> softmax weights sum to 1
+    for c in (1.0, -2.5):
+        vc = np.full(v.shape, c)
+        o, _ = O.sdpa(q, k, vc, causal=True, q_offset=5)
+        _close(o, np.full(o.shape, c), 4e-15 * abs(c), "constant values %g" % c)
+
+
+def pin_sdpa_structure(O):
+    """GQA == MHA on repeated K/V; no mask == causal at the last position; key order free without mask."""
+    rng = _rng(10)
+    B, H, Hkv, Lq, Lkv, D = 2, 8, 2, 3, 11, 4
+    q = rng.standard_normal((B, H, Lq, D)); k = rng.standard_normal((B, Hkv, Lkv, D))
+    v = rng.standard_normal((B, Hkv, Lkv, D))
+    o1, _ = O.sdpa(q, k, v, causal=True, q_offset=6)
+    kr = np.repeat(k, H // Hkv, axis=1); vr = np.repeat(v, H // Hkv, axis=1)
+    o2, _ = O.sdpa(q, kr, vr, causal=True, q_offset=6)
+    assert np.array_equal(o1, o2), "GQA == MHA with repeated heads"
+    q1 = q[:, :, :1].copy()
+    a, _ = O.sdpa(q1, k, v, causal=False, q_offset=0)
+    b, _ = O.sdpa(q1, k, v, causal=True, q_offset=Lkv - 1)
+    assert np.array_equal(a, b), "no mask == causal at the last position"
+    perm = rng.permutation(Lkv)
+    a, nrm = O.sdpa(q, k, v, causal=False, q_offset=0)
+    b, _ = O.sdpa(q, k[:, :, perm], v[:, :, perm], causal=False, q_offset=0)
+    _close(a, b, 8 * Lkv * U64 * nrm + 1e-300, "key permutation without mask")
+
+
+# ------------------------------------------------------------------ glue pins
+
+def pin_rmsnorm(O):
+    rng = _rng(11)
+    x = rng.standard_normal((6, 40)); w = rng.standard_normal(40)
+    y = O.rmsnorm(x, w, 1e-6)
+    want = F.rms_norm(torch.from_numpy(x), (40,), torch.from_numpy(w), 1e-6).numpy()
+    _close(y, want, 1e-14 * np.abs(want).max(), "rmsnorm vs torch")
+    for c in (3.0, -0.5):
+        xc = np.full((1, 40), c)
+        y = O.rmsnorm(xc, w, 1e-6)
+        _close(y[0], c / math.sqrt(c * c + 1e-6) * w, 1e-15 * np.abs(w).max(), "rmsnorm constant row")
+
+
+def pin_rope(O):
+    rng = _rng(12)
+    T, nh, D = 5, 3, 16
+    x = rng.standard_normal((T, nh, D))
+    y = O.rope(x, np.zeros(T, dtype=np.int64))
+    assert np.array_equal(y, x), "rope at position 0 is the identity"
+    pos = np.array([1, 7, 100, 4095, 8191])
+    y = O.rope(x, pos)
+    half = D // 2
+    z = x[..., :half] + 1j * x[..., half:]
+    inv = 10000.0 ** (-2.0 * np.arange(half) / D)
+    zr = z * np.exp(1j * pos[:, None, None] * inv[None, None, :])
+    _close(y[..., :half], zr.real, 1e-12, "rope real part (complex form)")
+    _close(y[..., half:], zr.imag, 1e-12, "rope imaginary part (complex form)")
+    y2 = O.rope(O.rope(x, np.full(T, 3)), np.full(T, 4))
+    _close(y2, O.rope(x, np.full(T, 7)), 1e-13, "rope composition 3+4 == 7")
+
+
+def pin_swiglu(O):
+    rng = _rng(13)
+    gu = rng.standard_normal((4, 2 * 24)) * 3
+    y = O.swiglu(gu)
+    g = torch.from_numpy(gu[:, :24]); u = torch.from_numpy(gu[:, 24:])
+    want = (F.silu(g) * u).numpy()
+    _close(y, want, 1e-15 * np.abs(want).max() + 1e-300, "swiglu vs torch silu")
+    gu0 = gu.copy(); gu0[:, :24] = 0.0
+    assert np.array_equal(O.swiglu(gu0), np.zeros((4, 24))), "silu(0) == 0"
+
+
+ALL_PINS = [pin_linear_bruteforce, pin_matmul_bruteforce, pin_addmm_bruteforce,
+            pin_gemm_integer_exact, pin_gemm_numpy, pin_gemm_identities,
+            pin_sdpa_bruteforce, pin_sdpa_torch, pin_sdpa_closed_forms, pin_sdpa_structure,
+            pin_rmsnorm, pin_rope, pin_swiglu]
