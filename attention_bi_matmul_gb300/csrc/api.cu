@@ -1,0 +1,444 @@
+// api.cu -- the C ABI of include/bi.h: argument validation, configuration
+// choice, tensor-map encoding and launches on the caller's stream.
+//
+// Routing rule (the batch-invariance contract): the kernel and its tile
+// configuration are functions of (dtype, N, K, weight layout) for GEMMs and of
+// (dtype, head_dim, group size, mask) for attention.  M, the batch, the query
+// length, the context length, pointer values and the environment never select
+// a different route; an argument the built kernels cannot take is an error,
+// never a fallback.
+#include <atomic>
+#include <cmath>
+#include <cstring>
+
+#include <cudaTypedefs.h>
+
+#include "internal.cuh"
+#include "ptx.cuh"
+
+namespace bi {
+
+// The device error word: written by kernels (atomicOr), read and cleared by
+// bi_last_device_error.  Static storage, one copy per device context.
+__device__ uint32_t g_error_word;
+
+namespace {
+
+std::atomic<int64_t> g_launches{0};
+
+constexpr int MAX_DEV = 64;
+uint32_t *g_err_ptr[MAX_DEV] = {};
+int g_sm_count[MAX_DEV] = {};
+int g_arch_ok[MAX_DEV] = {};  // 0 unknown, 1 sm_103, -1 other
+
+int current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    return (dev >= 0 && dev < MAX_DEV) ? dev : -1;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool load_encode() {
+    if (g_encode) return true;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+        return false;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return true;
+}
+
+// The code in this library is built for sm_103a only.
+bi_status check_device() {
+    const int dev = current_device();
+    if (dev < 0) return BI_ERR_CUDA;
+    if (g_arch_ok[dev] == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return BI_ERR_CUDA;
+        g_arch_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+    }
+    return g_arch_ok[dev] == 1 ? BI_OK : BI_ERR_UNSUPPORTED;
+}
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline int64_t esize(bi_dtype dt) { return dt == BI_F32 ? 4 : 2; }
+inline bool valid_dtype(bi_dtype dt) { return dt == BI_F32 || dt == BI_F16 || dt == BI_BF16; }
+
+// Common validation of the GEMM family.  Returns BI_OK to proceed.
+bi_status check_gemm(const void *a, int64_t lda, const void *b, int64_t ldb, void *y, int64_t ldy,
+                     int64_t M, int64_t N, int64_t K, bi_dtype dt, bool b_nk) {
+    if (!valid_dtype(dt)) return BI_ERR_UNSUPPORTED;
+    if (M < 0 || N <= 0 || K <= 0) return BI_ERR_INVALID_ARG;
+    if (!a || !b || !y) return BI_ERR_INVALID_ARG;
+    if (lda < K || ldy < N || (b_nk ? ldb < K : ldb < N)) return BI_ERR_INVALID_ARG;
+    if (M > (int64_t(1) << 31) || N > (int64_t(1) << 31) || K > (int64_t(1) << 31))
+        return BI_ERR_UNSUPPORTED;
+    if (dt != BI_F32) {
+        if (!aligned16(a) || !aligned16(b) || !aligned16(y)) return BI_ERR_ALIGNMENT;
+        if (lda % 8 || ldb % 8 || ldy % 8) return BI_ERR_ALIGNMENT;
+    } else {
+        if ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b) |
+             reinterpret_cast<uintptr_t>(y)) & 3u)
+            return BI_ERR_ALIGNMENT;
+    }
+    return BI_OK;
+}
+
+bi_status run_gemm(const void *a, int64_t lda, const void *b, int64_t ldb, bool b_nk,
+                   GemmArgs &args, bi_dtype dt, cudaStream_t s);
+
+}  // namespace
+
+// ------------------------------------------------------------------ helpers
+
+bi_status cuda_status(cudaError_t e) { return e == cudaSuccess ? BI_OK : BI_ERR_CUDA; }
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+uint32_t *device_error_word() {
+    const int dev = current_device();
+    if (dev < 0) return nullptr;
+    if (!g_err_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+        g_err_ptr[dev] = static_cast<uint32_t *>(p);
+    }
+    return g_err_ptr[dev];
+}
+
+int device_sm_count() {
+    const int dev = current_device();
+    if (dev < 0) return 1;
+    if (!g_sm_count[dev]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        g_sm_count[dev] = n > 0 ? n : 1;
+    }
+    return g_sm_count[dev];
+}
+
+bi_status encode_tmap(CUtensorMap *map, bi_dtype dt, int rank, void *base, const uint64_t *dims,
+                      const uint64_t *strides_bytes, const uint32_t *box, bool swizzle128) {
+    if (!load_encode()) return BI_ERR_CUDA;
+    const CUtensorMapDataType t = dt == BI_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                  : dt == BI_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    cuuint64_t gdim[5], gstr[4];
+    cuuint32_t bdim[5], estr[5];
+    for (int i = 0; i < rank; ++i) {
+        gdim[i] = dims[i];
+        bdim[i] = box[i];
+        estr[i] = 1;
+    }
+    for (int i = 0; i + 1 < rank; ++i) gstr[i] = strides_bytes[i];
+    const CUresult r = g_encode(map, t, static_cast<cuuint32_t>(rank), base, gdim, gstr, bdim, estr,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? BI_OK : BI_ERR_INVALID_ARG;
+}
+
+// Tile width of the tensor-core GEMM for (N, K, dtype, layout).  M is not an
+// input.  The width is the widest of the built ones that still gives one full
+// wave of tiles across the 152 SMs of a GB300 when M <= 128 (decode-shaped
+// calls are bandwidth-bound and need every SM streaming weights); the widest
+// tile is kept when even that leaves fewer than ~100 tiles.
+TcConfig tc_config(int64_t N, int64_t K, bi_dtype dt, bool b_mn_major) {
+    (void)K;
+    (void)dt;
+    static const int k_major_widths[] = {256, 128, 96, 64};
+    static const int mn_major_widths[] = {256, 128, 64};
+    const int *w = b_mn_major ? mn_major_widths : k_major_widths;
+    const int nw = b_mn_major ? 3 : 4;
+    constexpr int64_t SMS = 152;
+    int best = w[0];
+    double best_score = -1.0;
+    for (int i = 0; i < nw; ++i) {
+        const int64_t tiles = (N + w[i] - 1) / w[i];
+        const int64_t waves = (tiles + SMS - 1) / SMS;
+        const double fill = static_cast<double>(tiles) / static_cast<double>(waves * SMS);
+        // Narrower tiles cost tensor-core efficiency at large M: weight them.
+        const double eff = w[i] >= 256 ? 1.0 : w[i] >= 128 ? 0.9 : w[i] >= 96 ? 0.8 : 0.6;
+        const double score = fill * eff;
+        if (score > best_score + 1e-12) {
+            best_score = score;
+            best = w[i];
+        }
+    }
+    TcConfig c;
+    c.block_n = best;
+    c.stages = best <= 64 ? 8 : best <= 96 ? 7 : best <= 128 ? 6 : 4;
+    return c;
+}
+
+bi_status launch_gemm_tc_bf16(const void *a, int64_t lda, const void *b, int64_t ldb, bool b_nk,
+                              const GemmArgs &args, const TcConfig &cfg, cudaStream_t s);
+bi_status launch_gemm_tc_f16(const void *a, int64_t lda, const void *b, int64_t ldb, bool b_nk,
+                             const GemmArgs &args, const TcConfig &cfg, cudaStream_t s);
+
+bi_status launch_gemm_tc(const void *a, int64_t lda, const void *b, int64_t ldb, bool b_nk,
+                         const GemmArgs &args, bi_dtype dt, const TcConfig &cfg, cudaStream_t s) {
+    if (dt == BI_BF16) return launch_gemm_tc_bf16(a, lda, b, ldb, b_nk, args, cfg, s);
+    if (dt == BI_F16) return launch_gemm_tc_f16(a, lda, b, ldb, b_nk, args, cfg, s);
+    return BI_ERR_UNSUPPORTED;
+}
+
+namespace {
+
+bi_status run_gemm(const void *a, int64_t lda, const void *b, int64_t ldb, bool b_nk,
+                   GemmArgs &args, bi_dtype dt, cudaStream_t s) {
+    if (args.M == 0) return BI_OK;
+    bi_status st = check_device();
+    if (st != BI_OK) return st;
+    args.err = device_error_word();
+    if (!args.err) return BI_ERR_CUDA;
+    if (dt == BI_F32)
+        return launch_gemm_f32(static_cast<const float *>(a), lda, static_cast<const float *>(b),
+                               ldb, b_nk, args, s);
+    const TcConfig cfg = tc_config(args.N, args.K, dt, !b_nk);
+    return launch_gemm_tc(a, lda, b, ldb, b_nk, args, dt, cfg, s);
+}
+
+}  // namespace
+
+}  // namespace bi
+
+using namespace bi;
+
+extern "C" {
+
+bi_status bi_linear(const void *x, int64_t ldx, const void *w, int64_t ldw, const void *bias,
+                    void *y, int64_t ldy, int64_t M, int64_t N, int64_t K, bi_dtype dtype,
+                    bi_stream_t stream) {
+    bi_status st = check_gemm(x, ldx, w, ldw, y, ldy, M, N, K, dtype, true);
+    if (st != BI_OK) return st;
+    GemmArgs args{};
+    args.M = M; args.N = N; args.K = K; args.y = y; args.ldy = ldy;
+    args.bias = bias;
+    args.epi = bias ? EPI_BIAS : EPI_NONE;
+    return run_gemm(x, ldx, w, ldw, true, args, dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+bi_status bi_matmul(const void *a, int64_t lda, const void *b, int64_t ldb, void *y, int64_t ldy,
+                    int64_t M, int64_t N, int64_t K, bi_dtype dtype, bi_stream_t stream) {
+    bi_status st = check_gemm(a, lda, b, ldb, y, ldy, M, N, K, dtype, false);
+    if (st != BI_OK) return st;
+    GemmArgs args{};
+    args.M = M; args.N = N; args.K = K; args.y = y; args.ldy = ldy;
+    args.epi = EPI_NONE;
+    return run_gemm(a, lda, b, ldb, false, args, dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+bi_status bi_addmm(const void *c, int64_t ldc, const void *a, int64_t lda, const void *b,
+                   int64_t ldb, void *y, int64_t ldy, int64_t M, int64_t N, int64_t K, float alpha,
+                   float beta, bi_dtype dtype, bi_stream_t stream) {
+    bi_status st = check_gemm(a, lda, b, ldb, y, ldy, M, N, K, dtype, false);
+    if (st != BI_OK) return st;
+    if (!c || ldc < 0 || (ldc > 0 && ldc < N)) return BI_ERR_INVALID_ARG;
+    if (!std::isfinite(alpha) || !std::isfinite(beta)) return BI_ERR_INVALID_ARG;
+    GemmArgs args{};
+    args.M = M; args.N = N; args.K = K; args.y = y; args.ldy = ldy;
+    args.c = c; args.ldc = ldc; args.alpha = alpha; args.beta = beta;
+    args.epi = EPI_ADDMM;
+    return run_gemm(a, lda, b, ldb, false, args, dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+bi_status bi_gemm_config(int64_t N, int64_t K, bi_dtype dtype, int b_layout, int *block_n,
+                         int *stages) {
+    if (N <= 0 || K <= 0 || (b_layout != 0 && b_layout != 1)) return BI_ERR_INVALID_ARG;
+    if (dtype != BI_F16 && dtype != BI_BF16) {
+        if (dtype != BI_F32) return BI_ERR_UNSUPPORTED;
+        if (block_n) *block_n = 64;   // SIMT path: fixed 64 x 64 block tiles
+        if (stages) *stages = 1;
+        return BI_OK;
+    }
+    const TcConfig c = tc_config(N, K, dtype, b_layout == 1);
+    if (block_n) *block_n = c.block_n;
+    if (stages) *stages = c.stages;
+    return BI_OK;
+}
+
+bi_status bi_sdpa(const void *q, const int64_t qs[4], const void *k, const int64_t ks[4],
+                  const void *v, const int64_t vs[4], void *o, const int64_t os[4], int64_t B,
+                  int64_t H, int64_t Hkv, int64_t Lq, int64_t Lkv, int64_t D, float scale,
+                  bi_mask mask, int64_t q_offset, bi_dtype dtype, bi_stream_t stream) {
+    if (dtype != BI_BF16 && dtype != BI_F16) return valid_dtype(dtype) ? BI_ERR_UNSUPPORTED
+                                                                         : BI_ERR_UNSUPPORTED;
+    if (!q || !k || !v || !o || !qs || !ks || !vs || !os) return BI_ERR_INVALID_ARG;
+    if (B < 0 || H <= 0 || Hkv <= 0 || Lq < 0 || Lkv < 0 || D <= 0) return BI_ERR_INVALID_ARG;
+    if (H % Hkv) return BI_ERR_INVALID_ARG;
+    if (mask != BI_MASK_CAUSAL && mask != BI_MASK_NONE) return BI_ERR_UNSUPPORTED;
+    if (q_offset < 0) q_offset = Lkv - Lq;
+    if (q_offset < 0 || q_offset + Lq > Lkv) return BI_ERR_INVALID_ARG;
+    if (Lq == 0 || B == 0) return BI_OK;
+    if (D != 128) return BI_ERR_UNSUPPORTED;
+    const int64_t G = H / Hkv;
+    if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return BI_ERR_UNSUPPORTED;
+    if (qs[3] != 1 || ks[3] != 1 || vs[3] != 1 || os[3] != 1) return BI_ERR_INVALID_ARG;
+    for (int i = 0; i < 3; ++i)
+        if (qs[i] < 0 || ks[i] < 0 || vs[i] < 0 || os[i] < 0) return BI_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return BI_ERR_ALIGNMENT;
+    for (int i = 0; i < 3; ++i)
+        if (qs[i] % 8 || ks[i] % 8 || vs[i] % 8 || os[i] % 8) return BI_ERR_ALIGNMENT;
+    if (Lkv > (int64_t(1) << 31) || Lq > (int64_t(1) << 31)) return BI_ERR_UNSUPPORTED;
+    bi_status st = check_device();
+    if (st != BI_OK) return st;
+
+    SdpaArgs a{};
+    a.B = B; a.H = H; a.Hkv = Hkv; a.Lq = Lq; a.Lkv = Lkv; a.q_offset = q_offset;
+    a.group = static_cast<int>(G);
+    a.qt = static_cast<int>(128 / G);
+    a.causal = mask == BI_MASK_CAUSAL ? 1 : 0;
+    const double sc = scale > 0.0f ? static_cast<double>(scale) : 1.0 / std::sqrt(static_cast<double>(D));
+    a.scale_log2 = static_cast<float>(sc * 1.4426950408889634);   // scale * log2(e)
+    a.o = o;
+    for (int i = 0; i < 4; ++i) a.os[i] = os[i];
+    a.err = device_error_word();
+    if (!a.err) return BI_ERR_CUDA;
+
+    CUtensorMap tq, tk, tv;
+    {
+        const uint64_t dims[4] = {static_cast<uint64_t>(D), static_cast<uint64_t>(H),
+                                  static_cast<uint64_t>(Lq), static_cast<uint64_t>(B)};
+        const uint64_t str[3] = {static_cast<uint64_t>(qs[1]) * 2, static_cast<uint64_t>(qs[2]) * 2,
+                                 static_cast<uint64_t>(qs[0]) * 2};
+        const uint32_t box[4] = {64, static_cast<uint32_t>(G), static_cast<uint32_t>(128 / G), 1};
+        st = encode_tmap(&tq, dtype, 4, const_cast<void *>(q), dims, str, box, true);
+        if (st != BI_OK) return st;
+    }
+    {
+        const uint64_t dims[4] = {static_cast<uint64_t>(D), static_cast<uint64_t>(Lkv),
+                                  static_cast<uint64_t>(Hkv), static_cast<uint64_t>(B)};
+        const uint32_t box[4] = {64, 128, 1, 1};
+        const uint64_t sk[3] = {static_cast<uint64_t>(ks[2]) * 2, static_cast<uint64_t>(ks[1]) * 2,
+                                static_cast<uint64_t>(ks[0]) * 2};
+        st = encode_tmap(&tk, dtype, 4, const_cast<void *>(k), dims, sk, box, true);
+        if (st != BI_OK) return st;
+        const uint64_t sv[3] = {static_cast<uint64_t>(vs[2]) * 2, static_cast<uint64_t>(vs[1]) * 2,
+                                static_cast<uint64_t>(vs[0]) * 2};
+        st = encode_tmap(&tv, dtype, 4, const_cast<void *>(v), dims, sv, box, true);
+        if (st != BI_OK) return st;
+    }
+    return launch_sdpa(tq, tk, tv, a, dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+bi_status bi_rmsnorm(const void *x, int64_t ldx, const void *w, void *y, int64_t ldy, int64_t M,
+                     int64_t N, float eps, bi_dtype dtype, bi_stream_t stream) {
+    if (!valid_dtype(dtype)) return BI_ERR_UNSUPPORTED;
+    if (!x || !w || !y || M < 0 || N <= 0 || ldx < N || ldy < N) return BI_ERR_INVALID_ARG;
+    if (!(eps >= 0.0f) || !std::isfinite(eps)) return BI_ERR_INVALID_ARG;
+    if (M == 0) return BI_OK;
+    bi_status st = check_device();
+    if (st != BI_OK) return st;
+    return launch_rmsnorm(x, ldx, w, y, ldy, M, N, eps, dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+bi_status bi_rope(const void *x, const int64_t xs[4], void *y, const int64_t ys[4], int64_t B,
+                  int64_t L, int64_t nh, int64_t D, int64_t pos0, float base, bi_dtype dtype,
+                  bi_stream_t stream) {
+    if (dtype != BI_BF16 && dtype != BI_F16) return BI_ERR_UNSUPPORTED;
+    if (!x || !y || !xs || !ys || B < 0 || L < 0 || nh <= 0 || D <= 0 || (D & 1) || pos0 < 0)
+        return BI_ERR_INVALID_ARG;
+    if (!(base > 1.0f) || !std::isfinite(base)) return BI_ERR_INVALID_ARG;
+    if (xs[3] != 1 || ys[3] != 1) return BI_ERR_INVALID_ARG;
+    if (B == 0 || L == 0) return BI_OK;
+    bi_status st = check_device();
+    if (st != BI_OK) return st;
+    return launch_rope(x, xs, y, ys, B, L, nh, D, pos0, base, dtype,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+bi_status bi_swiglu(const void *gu, int64_t ldgu, void *y, int64_t ldy, int64_t M, int64_t I,
+                    bi_dtype dtype, bi_stream_t stream) {
+    if (!valid_dtype(dtype)) return BI_ERR_UNSUPPORTED;
+    if (!gu || !y || M < 0 || I <= 0 || ldgu < 2 * I || ldy < I) return BI_ERR_INVALID_ARG;
+    if (M == 0) return BI_OK;
+    bi_status st = check_device();
+    if (st != BI_OK) return st;
+    return launch_swiglu(gu, ldgu, y, ldy, M, I, dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+bi_status bi_add(const void *a, const void *b, void *y, int64_t n, bi_dtype dtype,
+                 bi_stream_t stream) {
+    if (!valid_dtype(dtype)) return BI_ERR_UNSUPPORTED;
+    if (!a || !b || !y || n < 0) return BI_ERR_INVALID_ARG;
+    if (n == 0) return BI_OK;
+    bi_status st = check_device();
+    if (st != BI_OK) return st;
+    return launch_add(a, b, y, n, dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+bi_status bi_embedding(const int64_t *ids, int64_t n_ids, const void *table, int64_t ldt,
+                       int64_t vocab, void *y, int64_t ldy, int64_t dim, bi_dtype dtype,
+                       bi_stream_t stream) {
+    if (!valid_dtype(dtype)) return BI_ERR_UNSUPPORTED;
+    if (!ids || !table || !y || n_ids < 0 || vocab <= 0 || dim <= 0 || ldt < dim || ldy < dim)
+        return BI_ERR_INVALID_ARG;
+    if (n_ids == 0) return BI_OK;
+    bi_status st = check_device();
+    if (st != BI_OK) return st;
+    if (!device_error_word()) return BI_ERR_CUDA;
+    return launch_embedding(ids, n_ids, table, ldt, vocab, y, ldy, dim, dtype,
+                            reinterpret_cast<cudaStream_t>(stream));
+}
+
+bi_status bi_copy4d(const void *src, const int64_t ss[4], void *dst, const int64_t ds[4],
+                    const int64_t n[4], bi_dtype dtype, bi_stream_t stream) {
+    if (!valid_dtype(dtype)) return BI_ERR_UNSUPPORTED;
+    if (!src || !dst || !ss || !ds || !n) return BI_ERR_INVALID_ARG;
+    for (int i = 0; i < 4; ++i)
+        if (n[i] < 0 || ss[i] < 0 || ds[i] < 0) return BI_ERR_INVALID_ARG;
+    if (ss[3] != 1 || ds[3] != 1) return BI_ERR_INVALID_ARG;
+    if (n[0] * n[1] * n[2] * n[3] == 0) return BI_OK;
+    bi_status st = check_device();
+    if (st != BI_OK) return st;
+    return launch_copy4d(src, ss, dst, ds, n, dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+const char *bi_status_string(bi_status status) {
+    switch (status) {
+        case BI_OK: return "BI_OK";
+        case BI_ERR_INVALID_ARG: return "BI_ERR_INVALID_ARG: invalid argument";
+        case BI_ERR_UNSUPPORTED: return "BI_ERR_UNSUPPORTED: configuration not built";
+        case BI_ERR_ALIGNMENT: return "BI_ERR_ALIGNMENT: pointer or stride not 16-byte aligned";
+        case BI_ERR_CUDA: return "BI_ERR_CUDA: CUDA runtime or driver error";
+        case BI_ERR_TIMEOUT: return "BI_ERR_TIMEOUT: a device-side bounded wait ran out";
+        default: return "unknown bi_status";
+    }
+}
+
+int bi_version(void) { return 100; }   // 0.1.0
+
+bi_status bi_last_device_error(bi_stream_t stream, uint32_t *code) {
+    uint32_t *p = device_error_word();
+    if (!p) return BI_ERR_CUDA;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return BI_ERR_CUDA;
+    uint32_t w = 0;
+    if (cudaMemcpy(&w, p, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess) return BI_ERR_CUDA;
+    const uint32_t zero = 0;
+    if (cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+        return BI_ERR_CUDA;
+    if (code) *code = w;
+    if (w & ERR_TIMEOUT) return BI_ERR_TIMEOUT;
+    if (w & ERR_BAD_INDEX) return BI_ERR_INVALID_ARG;
+    return w ? BI_ERR_CUDA : BI_OK;
+}
+
+int64_t bi_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+bi_status bi_debug_wait_probe(int64_t limit_us, bi_stream_t stream) {
+    if (limit_us < 1 || limit_us > 2000000) return BI_ERR_INVALID_ARG;
+    bi_status st = check_device();
+    if (st != BI_OK) return st;
+    if (!device_error_word()) return BI_ERR_CUDA;
+    return launch_wait_probe(limit_us, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,363 @@
+// gemm_tc.cuh -- batch-invariant 16-bit GEMM on the 5th-generation tensor cores.
+//
+// "mlx-batch-invariant" README, "How the kernels work" / GEMM: one block owns
+// the whole K reduction of its output tile, the K loop's trip count depends
+// on K alone, and a given row always lands at the same place in the same tile,
+// so nothing about the summation order can move when M changes; no split-K,
+// no atomics, fp32 accumulators, bias added into the accumulator and rounded
+// once.  The GB300 form of that rule:
+//
+//   * output tile 128 x BN (BN chosen from (dtype, N, K, layout) only), one
+//     tcgen05.mma accumulator in tensor memory per tile;
+//   * K visited in ascending 64-wide blocks, each as four K=16 MMAs in
+//     ascending order, always starting from a zero accumulator -- for every M;
+//   * operands staged by TMA into a multi-stage shared-memory ring with
+//     128-byte swizzle (rows beyond M or K are zero-filled by the copy engine,
+//     which adds exact zeros);
+//   * epilogue: tcgen05.ld of the fp32 accumulator, + bias / alpha,beta*c in
+//     fp32 in a fixed order, one rounding to the output dtype.
+//
+// Roles (192 threads, persistent over output tiles):
+//   warp 0 lane 0  TMA producer
+//   warp 1         TMEM allocation; lane 0 issues the MMAs
+//   warps 2..5     epilogue (warp w reads TMEM lanes 32*(w%4) .. +31)
+// Two accumulator buffers in TMEM let the epilogue of tile i overlap the
+// mainloop of tile i+1.  The order in which tiles are visited never changes
+// any bit of the result.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.cuh"
+#include "ptx.cuh"
+
+namespace bi {
+
+template <typename T> __device__ __forceinline__ float to_f32(T x);
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
+    return __bfloat162float(x);
+}
+template <> __device__ __forceinline__ float to_f32<__half>(__half x) { return __half2float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+template <> __device__ __forceinline__ __half from_f32<__half>(float x) {
+    return __float2half_rn(x);
+}
+
+template <typename T> struct IsBf16 { static constexpr bool value = false; };
+template <> struct IsBf16<__nv_bfloat16> { static constexpr bool value = true; };
+
+// Pack 8 consecutive fp32 values into 8 16-bit values (16 bytes).
+template <typename T>
+__device__ __forceinline__ uint4 pack8(const float *v) {
+    union {
+        T h[8];
+        uint4 u;
+    } p;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) p.h[i] = from_f32<T>(v[i]);
+    return p.u;
+}
+
+// Epilogue of 32 consecutive output columns [n0, n0+32) of row m.
+template <typename T>
+__device__ __forceinline__ void gemm_epilogue32(const uint32_t (&r)[32], int64_t m, int64_t n0,
+                                                const GemmArgs &a) {
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+    const int64_t N = a.N;
+    if (a.epi == EPI_BIAS) {
+        const T *bias = static_cast<const T *>(a.bias);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (n0 + i < N) v[i] = __fadd_rn(v[i], to_f32<T>(bias[n0 + i]));
+    } else if (a.epi == EPI_ADDMM) {
+        const T *crow = static_cast<const T *>(a.c) + (a.ldc ? m * a.ldc : 0);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (n0 + i < N)
+                v[i] = __fadd_rn(__fmul_rn(a.alpha, v[i]), __fmul_rn(a.beta, to_f32<T>(crow[n0 + i])));
+    }
+    T *yrow = static_cast<T *>(a.y) + m * a.ldy;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        const int64_t n = n0 + 8 * g;
+        if (n + 8 <= N) {
+            *reinterpret_cast<uint4 *>(yrow + n) = pack8<T>(v + 8 * g);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (n + i < N) yrow[n + i] = from_f32<T>(v[8 * g + i]);
+        }
+    }
+}
+
+constexpr int TC_BM = 128;
+constexpr int TC_BK = 64;
+constexpr int TC_THREADS = 192;
+constexpr int TC_GROUP_M = 8;
+
+__host__ __device__ constexpr uint32_t tc_tmem_cols(int bn) {
+    // two accumulator buffers of bn fp32 columns, rounded up to a power of two >= 32
+    return (2 * bn <= 32) ? 32u : (2 * bn <= 64) ? 64u : (2 * bn <= 128) ? 128u
+           : (2 * bn <= 256) ? 256u : 512u;
+}
+
+template <int BN, int STAGES>
+__host__ __device__ constexpr size_t tc_smem_bytes() {
+    return 1024 /* alignment slack */ + (size_t)STAGES * (TC_BM * TC_BK * 2 + BN * TC_BK * 2) +
+           256 /* barriers etc */;
+}
+
+// Tile t -> (m block, n block), grouped so that concurrently running tiles share A and B in L2.
+__device__ __forceinline__ void tc_tile_coords(int64_t t, int64_t num_m, int64_t num_n,
+                                               int64_t &mb, int64_t &nb) {
+    const int64_t in_group = (int64_t)TC_GROUP_M * num_n;
+    const int64_t g = t / in_group;
+    const int64_t first_m = g * TC_GROUP_M;
+    const int64_t gm = (num_m - first_m) < TC_GROUP_M ? (num_m - first_m) : TC_GROUP_M;
+    const int64_t r = t - g * in_group;
+    mb = first_m + r % gm;
+    nb = r / gm;
+}
+
+template <typename T, int BN, int STAGES, bool B_MN>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmArgs args) {
+    constexpr uint32_t A_BYTES = TC_BM * TC_BK * 2;
+    constexpr uint32_t B_BYTES = BN * TC_BK * 2;
+    constexpr uint32_t TMEM_COLS = tc_tmem_cols(BN);
+    constexpr uint32_t IDESC = mma_idesc(IsBf16<T>::value, TC_BM, BN, B_MN);
+    static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile width");
+    static_assert(!B_MN || BN % 64 == 0, "MN-major B needs 64-column atoms");
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + STAGES * A_BYTES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(sB + STAGES * B_BYTES);
+    uint64_t *empty = full + STAGES;
+    uint64_t *tfull = empty + STAGES;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *mma_done = tempty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    const int64_t M = args.M, N = args.N, K = args.K;
+    const int64_t num_m = (M + TC_BM - 1) / TC_BM;
+    const int64_t num_n = (N + BN - 1) / BN;
+    const int64_t total = num_m * num_n;
+    const int KB = static_cast<int>((K + TC_BK - 1) / TC_BK);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 4);
+        }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            prefetch_tmap(&tmA);
+            prefetch_tmap(&tmB);
+            uint32_t it = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; ok && t < total; t += gridDim.x) {
+                int64_t mb, nb;
+                tc_tile_coords(t, num_m, num_n, mb, nb);
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const uint32_t s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1u;
+                    if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&full[s], A_BYTES + B_BYTES);
+                    tma_load_2d(sA + s * A_BYTES, &tmA, &full[s], kb * TC_BK,
+                                static_cast<int32_t>(mb * TC_BM));
+                    if (!B_MN) {
+                        tma_load_2d(sB + s * B_BYTES, &tmB, &full[s], kb * TC_BK,
+                                    static_cast<int32_t>(nb * BN));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < BN / 64; ++j)
+                            tma_load_2d(sB + s * B_BYTES + j * 8192, &tmB, &full[s],
+                                        static_cast<int32_t>(nb * BN + j * 64), kb * TC_BK);
+                    }
+                }
+            }
+            if (!ok) {
+                // Let every copy already issued land before the block can exit.
+                const uint32_t first = it > STAGES ? it - STAGES : 0;
+                for (uint32_t i = first; i < it; ++i)
+                    mbar_wait_limited(&full[i % STAGES], (i / STAGES) & 1u, WAIT_LIMIT_NS);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            uint32_t it = 0, tc = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; ok && t < total; t += gridDim.x, ++tc) {
+                const uint32_t acc = tc & 1u;
+                const uint32_t aph = (tc >> 1) & 1u;
+                if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const uint32_t s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1u;
+                    if (!mbar_wait(&full[s], ph, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(sA + s * A_BYTES);
+                    const uint32_t b_addr = smem_u32(sB + s * B_BYTES);
+#pragma unroll
+                    for (int j = 0; j < TC_BK / 16; ++j) {
+                        const uint64_t ad = smem_desc(a_addr + j * 32, 16, 1024);
+                        const uint64_t bd = B_MN ? smem_desc(b_addr + j * 2048, 8192, 1024)
+                                                 : smem_desc(b_addr + j * 32, 16, 1024);
+                        mma_f16_ss(d_tmem, ad, bd, IDESC, (kb | j) != 0 ? 1u : 0u);
+                    }
+                    mma_commit(&empty[s]);
+                }
+                if (!ok) break;
+                mma_commit(&tfull[acc]);
+            }
+            // All issued MMAs must be complete before TMEM is released.
+            mma_commit(mma_done);
+            mbar_wait_limited(mma_done, 0, WAIT_LIMIT_NS);
+        }
+    } else {
+        // ------------------------------------------------ epilogue (warps 2..5)
+        const uint32_t quarter = static_cast<uint32_t>(warp & 3);
+        const int row_in_tile = static_cast<int>(quarter) * 32 + lane;
+        uint32_t tc = 0;
+        for (int64_t t = blockIdx.x; t < total; t += gridDim.x, ++tc) {
+            int64_t mb, nb;
+            tc_tile_coords(t, num_m, num_n, mb, nb);
+            const uint32_t acc = tc & 1u;
+            const uint32_t aph = (tc >> 1) & 1u;
+            if (!warp_wait(&tfull[acc], aph, abort_flag)) break;
+            tc_fence_after();
+            const int64_t m = mb * TC_BM + row_in_tile;
+#pragma unroll 1
+            for (int cc = 0; cc < BN / 32; ++cc) {
+                uint32_t r[32];
+                tmem_ld32(tmem_base + ((quarter * 32u) << 16) + acc * BN + cc * 32, r);
+                tmem_wait_ld(r);
+                if (m < M) gemm_epilogue32<T>(r, m, nb * BN + cc * 32, args);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+    if (threadIdx.x == 0 && *abort_flag) atomicOr(args.err, ERR_TIMEOUT);
+}
+
+// Host side: instantiate and launch one configuration.
+template <typename T, int BN, bool B_MN>
+bi_status launch_tc_inst(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &args,
+                         int stages_req, cudaStream_t s) {
+    // Stage count is a function of BN only (chosen so the ring fills ~190 KB).
+    constexpr int STAGES = (BN <= 64) ? 8 : (BN <= 96) ? 7 : (BN <= 128) ? 6 : 4;
+    (void)stages_req;
+    constexpr size_t SMEM = tc_smem_bytes<BN, STAGES>();
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (!attr_set[dev & 63]) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<T, BN, STAGES, B_MN>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(SMEM));
+        if (e != cudaSuccess) return cuda_status(e);
+        attr_set[dev & 63] = true;
+    }
+    const int64_t tiles = ((args.M + TC_BM - 1) / TC_BM) * ((args.N + BN - 1) / BN);
+    const int sms = device_sm_count();
+    const int grid = static_cast<int>(tiles < sms ? tiles : sms);
+    gemm_tc_kernel<T, BN, STAGES, B_MN><<<grid, TC_THREADS, SMEM, s>>>(ta, tb, args);
+    count_launch();
+    return cuda_status(cudaGetLastError());
+}
+
+template <int BN>
+constexpr int tc_stages_for() {
+    return (BN <= 64) ? 8 : (BN <= 96) ? 7 : (BN <= 128) ? 6 : 4;
+}
+
+// Dispatch on the configured tile width; builds the tensor maps.
+template <typename T>
+bi_status launch_gemm_tc_typed(const void *a, int64_t lda, const void *b, int64_t ldb, bool b_nk,
+                               const GemmArgs &args, bi_dtype dt, const TcConfig &cfg,
+                               cudaStream_t s) {
+    const int BN = cfg.block_n;
+    CUtensorMap ta, tb;
+    {
+        const uint64_t dims[2] = {static_cast<uint64_t>(args.K), static_cast<uint64_t>(args.M)};
+        const uint64_t strides[1] = {static_cast<uint64_t>(lda) * 2};
+        const uint32_t box[2] = {TC_BK, TC_BM};
+        bi_status st = encode_tmap(&ta, dt, 2, const_cast<void *>(a), dims, strides, box, true);
+        if (st != BI_OK) return st;
+    }
+    if (b_nk) {
+        const uint64_t dims[2] = {static_cast<uint64_t>(args.K), static_cast<uint64_t>(args.N)};
+        const uint64_t strides[1] = {static_cast<uint64_t>(ldb) * 2};
+        const uint32_t box[2] = {TC_BK, static_cast<uint32_t>(BN)};
+        bi_status st = encode_tmap(&tb, dt, 2, const_cast<void *>(b), dims, strides, box, true);
+        if (st != BI_OK) return st;
+    } else {
+        const uint64_t dims[2] = {static_cast<uint64_t>(args.N), static_cast<uint64_t>(args.K)};
+        const uint64_t strides[1] = {static_cast<uint64_t>(ldb) * 2};
+        const uint32_t box[2] = {64, TC_BK};
+        bi_status st = encode_tmap(&tb, dt, 2, const_cast<void *>(b), dims, strides, box, true);
+        if (st != BI_OK) return st;
+    }
+    if (b_nk) {
+        switch (BN) {
+            case 64: return launch_tc_inst<T, 64, false>(ta, tb, args, cfg.stages, s);
+            case 96: return launch_tc_inst<T, 96, false>(ta, tb, args, cfg.stages, s);
+            case 128: return launch_tc_inst<T, 128, false>(ta, tb, args, cfg.stages, s);
+            case 256: return launch_tc_inst<T, 256, false>(ta, tb, args, cfg.stages, s);
+            default: return BI_ERR_UNSUPPORTED;
+        }
+    } else {
+        switch (BN) {
+            case 64: return launch_tc_inst<T, 64, true>(ta, tb, args, cfg.stages, s);
+            case 128: return launch_tc_inst<T, 128, true>(ta, tb, args, cfg.stages, s);
+            case 256: return launch_tc_inst<T, 256, true>(ta, tb, args, cfg.stages, s);
+            default: return BI_ERR_UNSUPPORTED;
+        }
+    }
+}
+
+}  // namespace bi

@@ -1,0 +1,79 @@
+// internal.cuh -- declarations shared by the library's translation units.
+// Not part of the public ABI (that is include/bi.h).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/bi.h"
+
+namespace bi {
+
+// Epilogue kinds of the GEMM kernels.
+enum Epilogue : int { EPI_NONE = 0, EPI_BIAS = 1, EPI_ADDMM = 2 };
+
+struct GemmArgs {
+    int64_t M, N, K;
+    void *y;
+    int64_t ldy;
+    const void *bias;  // EPI_BIAS
+    const void *c;     // EPI_ADDMM
+    int64_t ldc;       // 0: c is one row [N]
+    float alpha, beta; // EPI_ADDMM
+    int epi;
+    uint32_t *err;     // device error word
+};
+
+// Tile configuration of the tensor-core GEMM for one (N, K, dtype, layout).
+struct TcConfig {
+    int block_n;
+    int stages;
+};
+
+// ---- host helpers (api.cu)
+uint32_t *device_error_word();                   // per current device, cached
+int device_sm_count();                           // per current device, cached
+void count_launch();                             // launch counter
+bi_status encode_tmap(CUtensorMap *map, bi_dtype dt, int rank, void *base,
+                      const uint64_t *dims, const uint64_t *strides_bytes,
+                      const uint32_t *box, bool swizzle128);
+TcConfig tc_config(int64_t N, int64_t K, bi_dtype dt, bool b_mn_major);
+bi_status cuda_status(cudaError_t e);
+
+// ---- launchers
+bi_status launch_gemm_f32(const float *a, int64_t lda, const float *b, int64_t ldb, bool b_nk,
+                          const GemmArgs &args, cudaStream_t s);
+bi_status launch_gemm_tc(const void *a, int64_t lda, const void *b, int64_t ldb, bool b_nk,
+                         const GemmArgs &args, bi_dtype dt, const TcConfig &cfg, cudaStream_t s);
+
+struct SdpaArgs {
+    int64_t B, H, Hkv, Lq, Lkv, q_offset;
+    int group;         // H / Hkv
+    int qt;            // query positions per tile = 128 / group
+    int causal;
+    float scale_log2;  // scale * log2(e)
+    void *o;
+    int64_t os[4];
+    uint32_t *err;
+};
+bi_status launch_sdpa(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                      const SdpaArgs &args, bi_dtype dt, cudaStream_t s);
+
+bi_status launch_rmsnorm(const void *x, int64_t ldx, const void *w, void *y, int64_t ldy,
+                         int64_t M, int64_t N, float eps, bi_dtype dt, cudaStream_t s);
+bi_status launch_rope(const void *x, const int64_t xs[4], void *y, const int64_t ys[4],
+                      int64_t B, int64_t L, int64_t nh, int64_t D, int64_t pos0, float base,
+                      bi_dtype dt, cudaStream_t s);
+bi_status launch_swiglu(const void *gu, int64_t ldgu, void *y, int64_t ldy, int64_t M, int64_t I,
+                        bi_dtype dt, cudaStream_t s);
+bi_status launch_add(const void *a, const void *b, void *y, int64_t n, bi_dtype dt,
+                     cudaStream_t s);
+bi_status launch_embedding(const int64_t *ids, int64_t n_ids, const void *table, int64_t ldt,
+                           int64_t vocab, void *y, int64_t ldy, int64_t dim, bi_dtype dt,
+                           cudaStream_t s);
+bi_status launch_copy4d(const void *src, const int64_t ss[4], void *dst, const int64_t ds[4],
+                        const int64_t n[4], bi_dtype dt, cudaStream_t s);
+bi_status launch_wait_probe(int64_t limit_us, cudaStream_t s);
+
+}  // namespace bi

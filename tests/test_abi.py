@@ -1,0 +1,116 @@
+"""The C-ABI library builds, loads, exports every declared symbol, and rejects bad
+arguments on the host (CPU only: no call here reaches a kernel launch)."""
+import ctypes
+import subprocess
+
+import pytest
+
+from attention_bi_matmul_gb300 import _lib as L
+from attention_bi_matmul_gb300 import build as B
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return L.load()
+
+
+def test_header_matches_binding():
+    declared = L.header_functions()
+    assert sorted(set(declared)) == sorted(L.SIGNATURES), (
+        "include/bi.h and the ctypes signatures disagree")
+
+
+def test_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB], stdout=subprocess.PIPE,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    for name in L.header_functions():
+        assert name in exported, "%s is declared in include/bi.h but not exported" % name
+        assert getattr(lib, name) is not None
+
+
+def test_status_strings_and_version(lib):
+    for st in range(6):
+        s = lib.bi_status_string(st).decode()
+        assert s.startswith("BI_"), s
+    assert lib.bi_version() == 100
+
+
+def test_gemm_config_ignores_M_and_is_host_only(lib):
+    bn, st = ctypes.c_int(), ctypes.c_int()
+    for N in (512, 4096, 11008, 14336, 19456, 38912):
+        for layout in (0, 1):
+            assert lib.bi_gemm_config(N, 4096, L.BI_BF16, layout, ctypes.byref(bn),
+                                      ctypes.byref(st)) == L.BI_OK
+            assert bn.value in (64, 96, 128, 256) and st.value >= 4
+            if layout == 1:
+                assert bn.value % 64 == 0
+    assert lib.bi_gemm_config(14336, 4096, L.BI_BF16, 0, ctypes.byref(bn), None) == L.BI_OK
+    assert bn.value == 96
+    assert lib.bi_gemm_config(0, 4096, L.BI_BF16, 0, None, None) == L.BI_ERR_INVALID_ARG
+    assert lib.bi_gemm_config(64, 64, 7, 0, None, None) == L.BI_ERR_UNSUPPORTED
+
+
+def test_host_validation_rejects_before_launch(lib):
+    nul = None
+    p = ctypes.c_void_p(4096)  # never dereferenced: validation fails first
+    s = ctypes.c_void_p(0)
+    # null pointers / bad sizes
+    assert lib.bi_linear(nul, 8, p, 8, nul, p, 8, 1, 8, 8, L.BI_BF16, s) == L.BI_ERR_INVALID_ARG
+    assert lib.bi_linear(p, 8, p, 8, nul, p, 8, 1, 0, 8, L.BI_BF16, s) == L.BI_ERR_INVALID_ARG
+    assert lib.bi_linear(p, 8, p, 8, nul, p, 8, 1, 8, 0, L.BI_BF16, s) == L.BI_ERR_INVALID_ARG
+    assert lib.bi_linear(p, 4, p, 8, nul, p, 8, 1, 8, 8, L.BI_BF16, s) == L.BI_ERR_INVALID_ARG
+    # alignment of 16-bit operands: a pointer off by 2 bytes, a row stride not a multiple of 8
+    q = ctypes.c_void_p(4096 + 2)
+    assert lib.bi_matmul(q, 16, p, 16, p, 16, 2, 16, 16, L.BI_BF16, s) == L.BI_ERR_ALIGNMENT
+    assert lib.bi_matmul(p, 20, p, 16, p, 16, 2, 16, 20, L.BI_F16, s) == L.BI_ERR_ALIGNMENT
+    # unknown dtype
+    assert lib.bi_matmul(p, 16, p, 16, p, 16, 2, 16, 16, 9, s) == L.BI_ERR_UNSUPPORTED
+    # addmm: c must be given; ldc in (0, N) is invalid
+    assert lib.bi_addmm(nul, 0, p, 16, p, 16, p, 16, 2, 16, 16, 1.0, 1.0, L.BI_BF16, s) \
+        == L.BI_ERR_INVALID_ARG
+    assert lib.bi_addmm(p, 8, p, 16, p, 16, p, 16, 2, 16, 16, 1.0, 1.0, L.BI_BF16, s) \
+        == L.BI_ERR_INVALID_ARG
+    # M == 0 is a no-op
+    assert lib.bi_linear(p, 8, p, 8, nul, p, 8, 0, 8, 8, L.BI_BF16, s) == L.BI_OK
+
+
+def test_sdpa_validation(lib):
+    p = ctypes.c_void_p(4096)
+    s = ctypes.c_void_p(0)
+    st4 = L.i64arr([32 * 9 * 128, 9 * 128, 128, 1])
+    args = lambda **kw: dict(dict(B=1, H=4, Hkv=2, Lq=1, Lkv=9, D=128, scale=0.0,
+                                  mask=L.BI_MASK_CAUSAL, q_offset=-1, dt=L.BI_BF16), **kw)
+
+    def call(**kw):
+        a = args(**kw)
+        return lib.bi_sdpa(p, st4, p, st4, p, st4, p, st4, a["B"], a["H"], a["Hkv"], a["Lq"],
+                           a["Lkv"], a["D"], a["scale"], a["mask"], a["q_offset"], a["dt"], s)
+
+    assert call(H=3) == L.BI_ERR_INVALID_ARG                  # H % Hkv != 0
+    assert call(q_offset=9) == L.BI_ERR_INVALID_ARG           # q_offset + Lq > Lkv
+    assert call(Lq=10) == L.BI_ERR_INVALID_ARG                # default offset negative
+    assert call(mask=5) == L.BI_ERR_UNSUPPORTED
+    assert call(dt=L.BI_F32) == L.BI_ERR_UNSUPPORTED
+    assert call(D=64) == L.BI_ERR_UNSUPPORTED                 # head dim not built
+    assert call(H=64, Hkv=2) == L.BI_ERR_UNSUPPORTED          # group of 32 not built
+    assert call(Lq=0) == L.BI_OK                              # empty: no-op
+    bad = L.i64arr([32 * 9 * 128, 9 * 128, 128, 2])
+    assert lib.bi_sdpa(p, bad, p, st4, p, st4, p, st4, 1, 4, 2, 1, 9, 128, 0.0,
+                       L.BI_MASK_CAUSAL, -1, L.BI_BF16, s) == L.BI_ERR_INVALID_ARG
+
+
+def test_glue_validation(lib):
+    p = ctypes.c_void_p(4096)
+    s = ctypes.c_void_p(0)
+    assert lib.bi_rmsnorm(p, 8, p, p, 8, 1, 16, 1e-6, L.BI_BF16, s) == L.BI_ERR_INVALID_ARG
+    assert lib.bi_rmsnorm(p, 16, p, p, 16, 1, 16, -1.0, L.BI_BF16, s) == L.BI_ERR_INVALID_ARG
+    assert lib.bi_swiglu(p, 10, p, 8, 1, 8, L.BI_BF16, s) == L.BI_ERR_INVALID_ARG
+    x4 = L.i64arr([1024, 256, 128, 1])
+    assert lib.bi_rope(p, x4, p, x4, 1, 2, 2, 127, 0, 1e4, L.BI_BF16, s) == L.BI_ERR_INVALID_ARG
+    assert lib.bi_rope(p, x4, p, x4, 1, 2, 2, 128, 0, 1e4, L.BI_F32, s) == L.BI_ERR_UNSUPPORTED
+    assert lib.bi_embedding(None, 4, p, 8, 10, p, 8, 8, L.BI_BF16, s) == L.BI_ERR_INVALID_ARG
+    assert lib.bi_add(p, p, p, -1, L.BI_BF16, s) == L.BI_ERR_INVALID_ARG
+    assert lib.bi_debug_wait_probe(0, s) == L.BI_ERR_INVALID_ARG
+    assert lib.bi_debug_wait_probe(3000000, s) == L.BI_ERR_INVALID_ARG

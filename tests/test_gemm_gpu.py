@@ -1,0 +1,229 @@
+"""GEMM parity against the fp64 oracle and batch invariance, through the C ABI (GPU)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attention_bi_matmul_gb300 import synth
+from tolerances import assert_same_bits, bits, check_close, count_bit_diffs
+
+pytestmark = pytest.mark.gpu
+
+DT = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}
+
+
+@pytest.fixture(scope="module")
+def bi():
+    import __graft_entry__
+    __graft_entry__.build()
+    import attention_bi_matmul_gb300 as m
+    torch.cuda.set_device(0)
+    return m
+
+
+def _dev(*ts):
+    return [t.cuda() for t in ts]
+
+
+def _no_device_error(bi):
+    st, code = bi.last_device_error()
+    assert st == 0, "device error word %#x" % code
+
+
+# ------------------------------------------------------------------ fp32 linear (small config)
+
+def test_fp32_linear_rows_invariant_and_accurate(bi):
+    """x[M,256] . w[512,256]^T + bias, M in {1,2,3,4,8}: row 0 bit-identical across M,
+    every row within 1e-5 * sum|x w| of the fp64 oracle."""
+    outs = {}
+    for M in (1, 2, 3, 4, 8):
+        x, w, bias = synth.linear_f32(M, seed=0)
+        y = bi.linear(*_dev(x, w, bias))
+        ref, nrm = oracle.linear(x, w, bias)
+        check_close(y, ref, nrm, torch.float32, "fp32 linear M=%d" % M)
+        outs[M] = y
+    for M in (2, 3, 4, 8):
+        assert_same_bits(outs[M][:1], outs[1], "fp32 linear row 0, M=%d vs M=1" % M)
+        assert_same_bits(outs[M], outs[8][:M], "fp32 linear rows, M=%d vs M=8" % M)
+    _no_device_error(bi)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (70, 130, 90), (129, 65, 257), (5, 300, 33)])
+def test_fp32_matmul_addmm_ragged(bi, M, N, K):
+    a, b, c = synth.gemm16(M, N, K, "fp32", seed=3, with_c=True)
+    y = bi.matmul(*_dev(a, b))
+    ref, nrm = oracle.matmul(a, b)
+    check_close(y, ref, nrm, torch.float32, "fp32 matmul %s" % ((M, N, K),))
+    ya = bi.addmm(*_dev(c, a, b), alpha=0.5, beta=-1.5)
+    ref, nrm = oracle.addmm(c, a, b, 0.5, -1.5)
+    check_close(ya, ref, nrm, torch.float32, "fp32 addmm")
+    crow = c[0].contiguous()
+    yr = bi.addmm(*_dev(crow, a, b))
+    ref, nrm = oracle.addmm(crow, a, b)
+    check_close(yr, ref, nrm, torch.float32, "fp32 addmm row c")
+
+
+# ------------------------------------------------------------------ 16-bit parity, every tile width
+
+def _widths(bi):
+    """N values that select each built tile width (the width is a function of N)."""
+    out = {}
+    for layout, Ns in (("linear", (4096, 14336, 19456, 38912)), ("matmul", (4096, 19456, 38912))):
+        for N in Ns:
+            out.setdefault((layout, bi.gemm_config(N, 256, torch.bfloat16, layout)[0]), N)
+    return out
+
+
+@pytest.mark.parametrize("dt", ["bf16", "fp16"])
+def test_tile_widths_all_selected(bi, dt):
+    w = _widths(bi)
+    assert {bn for (lay, bn) in w if lay == "linear"} == {64, 96, 128, 256}
+    assert {bn for (lay, bn) in w if lay == "matmul"} == {64, 128, 256}
+
+
+@pytest.mark.parametrize("dt", ["bf16", "fp16"])
+@pytest.mark.parametrize("layout_bn", ["linear-64", "linear-96", "linear-128", "linear-256",
+                                       "matmul-64", "matmul-128", "matmul-256"])
+def test_16bit_parity_each_width(bi, dt, layout_bn):
+    layout, bn = layout_bn.split("-")
+    N = _widths(bi)[(layout, int(bn))]
+    M, K = 300, 200          # three row tiles (ragged), four K blocks (ragged last block)
+    # sample 640 output columns: the first tile, one in the middle, the ragged end
+    a, b, c = synth.gemm16(M, N, K, dt, seed=5, layout=layout, with_c=True)
+    ad, bd, cd = _dev(a, b, c)
+    if layout == "linear":
+        bias = synth.normal((N,), 6, 0.1, dt)
+        y = bi.linear(ad, bd, bias.cuda())
+        cols = np.r_[0:256, N // 2 - 64:N // 2 + 64, N - 256:N]
+        ref, nrm = oracle.linear(a, b[cols], bias[cols])
+        check_close(y[:, cols], ref, nrm, DT[dt], "linear bn=%s N=%d" % (bn, N))
+    else:
+        y = bi.matmul(ad, bd)
+        cols = np.r_[0:256, N // 2 - 64:N // 2 + 64, N - 256:N]
+        bs = b[:, cols].contiguous()
+        ref, nrm = oracle.matmul(a, bs)
+        check_close(y[:, cols], ref, nrm, DT[dt], "matmul bn=%s N=%d" % (bn, N))
+        ya = bi.addmm(cd, ad, bd, alpha=1.0, beta=1.0)
+        ref, nrm = oracle.addmm(c[:, cols].contiguous(), a, bs, 1.0, 1.0)
+        check_close(ya[:, cols], ref, nrm, DT[dt], "addmm bn=%s" % bn)
+        ya = bi.addmm(cd[0].contiguous(), ad, bd, alpha=-0.75, beta=2.0)
+        ref, nrm = oracle.addmm(c[0, cols].contiguous(), a, bs, -0.75, 2.0)
+        check_close(ya[:, cols], ref, nrm, DT[dt], "addmm row-c bn=%s" % bn)
+    _no_device_error(bi)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "fp16"])
+@pytest.mark.parametrize("M,N,K", [(1, 8, 8), (1, 40, 72), (17, 520, 1000), (128, 256, 64),
+                                   (129, 96, 4096), (3, 2056, 136)])
+def test_16bit_ragged_shapes(bi, dt, M, N, K):
+    """Sizes that are not multiples of the tiles: tails in M, N and K, tiny N and K."""
+    x, w = synth.gemm16(M, N, K, dt, seed=7, layout="linear")
+    y = bi.linear(*_dev(x, w))
+    ref, nrm = oracle.linear(x, w)
+    check_close(y, ref, nrm, DT[dt], "linear %s" % ((M, N, K),))
+    a, b = synth.gemm16(M, N, K, dt, seed=8, layout="matmul")
+    y = bi.matmul(*_dev(a, b))
+    ref, nrm = oracle.matmul(a, b)
+    check_close(y, ref, nrm, DT[dt], "matmul %s" % ((M, N, K),))
+
+
+def test_integer_exact_bits(bi):
+    """Small-integer operands: every partial sum is exact in fp32, so every dtype path and
+    the oracle agree exactly (pins the GEMM and its epilogue bits)."""
+    g = torch.Generator().manual_seed(21)
+    M, N, K = 130, 200, 96
+    a = torch.randint(-2, 3, (M, K), generator=g).float()
+    b = torch.randint(-2, 3, (K, N), generator=g).float()
+    c = torch.randint(-3, 4, (N,), generator=g).float()
+    want = torch.from_numpy(oracle.addmm(c, a, b, 1.0, 1.0)[0])
+    assert want.abs().max() <= 256
+    for dt in (torch.float32, torch.bfloat16, torch.float16):
+        ad, bd, cd = a.to(dt).cuda(), b.to(dt).cuda(), c.to(dt).cuda()
+        y = bi.addmm(cd, ad, bd).float().cpu().double()
+        assert torch.equal(y, want), "integer-exact addmm %s" % dt
+        y = bi.linear(ad, bd.t().contiguous(), cd).float().cpu().double()
+        assert torch.equal(y, want), "integer-exact linear %s" % dt
+
+
+# ------------------------------------------------------------------ the 16-bit batch-size config
+
+C2_M = (1, 2, 3, 4, 8, 16, 32, 64, 128, 256, 512)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "fp16"])
+@pytest.mark.parametrize("N", [4096, 11008, 14336])
+def test_c2_rows_invariant_across_batch(bi, dt, N):
+    """K=4096: every row's bits are the same for M in {1..512}, for matmul, addmm and linear,
+    and with different batch neighbours; sampled rows/columns match the oracle."""
+    K = 4096
+    a, b, c = synth.gemm16(512, N, K, dt, seed=1, with_c=True, device="cuda")
+    w = b.t().contiguous()
+    full_m = bi.matmul(a, b)
+    full_a = bi.addmm(c, a, b, alpha=1.0, beta=1.0)
+    full_l = bi.linear(a, w)
+    for M in C2_M:
+        assert_same_bits(bi.matmul(a[:M], b), full_m[:M], "matmul N=%d M=%d" % (N, M))
+        assert_same_bits(bi.addmm(c[:M], a[:M], b, alpha=1.0, beta=1.0), full_a[:M],
+                         "addmm N=%d M=%d" % (N, M))
+        assert_same_bits(bi.linear(a[:M], w), full_l[:M], "linear N=%d M=%d" % (N, M))
+    # batch neighbours: row 0 surrounded by other rows
+    perm = torch.randperm(511, generator=torch.Generator().manual_seed(2))[:63].cuda() + 1
+    mixed = torch.cat([a[:1], a[perm]], 0)
+    assert_same_bits(bi.matmul(mixed, b)[:1], full_m[:1], "matmul neighbours")
+    # accuracy on sampled rows
+    rows = [0, 1, 255, 511]
+    cols = np.r_[0:128, N - 128:N]
+    ah = a[rows].cpu()
+    bh = b[:, cols].contiguous().cpu()
+    ref, nrm = oracle.matmul(ah, bh)
+    check_close(full_m[rows][:, cols], ref, nrm, DT[dt], "matmul N=%d sampled" % N)
+    ref, nrm = oracle.addmm(c[rows][:, cols].cpu(), ah, bh, 1.0, 1.0)
+    check_close(full_a[rows][:, cols], ref, nrm, DT[dt], "addmm N=%d sampled" % N)
+    _no_device_error(bi)
+
+
+def test_c2_cublas_control_differs(bi):
+    """The negative control: torch.matmul (cuBLAS) changes a row's bits with the batch size
+    on at least one of the config's shapes, where the library's do not."""
+    K = 4096
+    diffs = 0
+    for dt in ("bf16", "fp16"):
+        for N in (4096, 11008, 14336):
+            a, b = synth.gemm16(512, N, K, dt, seed=1, device="cuda")
+            ref = torch.matmul(a[:1], b)
+            for M in C2_M[1:]:
+                diffs += count_bit_diffs(torch.matmul(a[:M], b)[:1], ref)
+    print("cuBLAS control: %d differing bit patterns in row 0 across the sweep" % diffs)
+    assert diffs > 0, "cuBLAS was batch-invariant on every shape of the sweep"
+
+
+def test_eager_vs_cuda_graph(bi):
+    """The same calls captured in a CUDA graph and replayed give the same bits."""
+    a, b, c = synth.gemm16(64, 4096, 4096, "bf16", seed=4, with_c=True, device="cuda")
+    w = b.t().contiguous()
+    eager = (bi.linear(a, w), bi.addmm(c, a, b))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        bi.linear(a, w)   # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    yl = torch.empty_like(eager[0])
+    ya = torch.empty_like(eager[1])
+    with torch.cuda.graph(g):
+        bi.linear(a, w, out=yl)
+        bi.addmm(c, a, b, out=ya)
+    g.replay()
+    torch.cuda.synchronize()
+    assert_same_bits(yl, eager[0], "linear graph vs eager")
+    assert_same_bits(ya, eager[1], "addmm graph vs eager")
+    g.replay()
+    torch.cuda.synchronize()
+    assert_same_bits(yl, eager[0], "linear graph replay 2")
+
+
+def test_repeated_runs_identical(bi):
+    a, b = synth.gemm16(200, 11008, 4096, "bf16", seed=9, device="cuda")
+    y0 = bi.matmul(a, b)
+    for _ in range(3):
+        assert_same_bits(bi.matmul(a, b), y0, "repeat")
