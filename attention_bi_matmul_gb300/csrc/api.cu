@@ -66,7 +66,6 @@ bi_status check_device() {
 }
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-inline int64_t esize(bi_dtype dt) { return dt == BI_F32 ? 4 : 2; }
 inline bool valid_dtype(bi_dtype dt) { return dt == BI_F32 || dt == BI_F16 || dt == BI_BF16; }
 
 // Common validation of the GEMM family.  Returns BI_OK to proceed.
@@ -145,35 +144,20 @@ bi_status encode_tmap(CUtensorMap *map, bi_dtype dt, int rank, void *base, const
 }
 
 // Tile width of the tensor-core GEMM for (N, K, dtype, layout).  M is not an
-// input.  The width is the widest of the built ones that still gives one full
-// wave of tiles across the 152 SMs of a GB300 when M <= 128 (decode-shaped
-// calls are bandwidth-bound and need every SM streaming weights); the widest
-// tile is kept when even that leaves fewer than ~100 tiles.
+// input, and neither is anything else about the call.  Measured on GB300
+// (bf16, weights streamed from HBM): at K = 4096 a 128-column tile is within a
+// few percent of the best width for every M from 1 to 512 (it keeps N/128
+// blocks streaming weights for decode-shaped calls), while at K = 8192 the
+// 256-column tile is best both for decode-shaped calls and at M = 8192
+// (1.6 PFLOP/s vs 1.1 for 128 columns).  Hence: 256 columns from K = 8192 up,
+// 128 below.  Both widths exist for both weight layouts.
 TcConfig tc_config(int64_t N, int64_t K, bi_dtype dt, bool b_mn_major) {
-    (void)K;
+    (void)N;
     (void)dt;
-    static const int k_major_widths[] = {256, 128, 96, 64};
-    static const int mn_major_widths[] = {256, 128, 64};
-    const int *w = b_mn_major ? mn_major_widths : k_major_widths;
-    const int nw = b_mn_major ? 3 : 4;
-    constexpr int64_t SMS = 152;
-    int best = w[0];
-    double best_score = -1.0;
-    for (int i = 0; i < nw; ++i) {
-        const int64_t tiles = (N + w[i] - 1) / w[i];
-        const int64_t waves = (tiles + SMS - 1) / SMS;
-        const double fill = static_cast<double>(tiles) / static_cast<double>(waves * SMS);
-        // Narrower tiles cost tensor-core efficiency at large M: weight them.
-        const double eff = w[i] >= 256 ? 1.0 : w[i] >= 128 ? 0.9 : w[i] >= 96 ? 0.8 : 0.6;
-        const double score = fill * eff;
-        if (score > best_score + 1e-12) {
-            best_score = score;
-            best = w[i];
-        }
-    }
+    (void)b_mn_major;
     TcConfig c;
-    c.block_n = best;
-    c.stages = best <= 64 ? 8 : best <= 96 ? 7 : best <= 128 ? 6 : 4;
+    c.block_n = K >= 8192 ? 256 : 128;
+    c.stages = c.block_n == 256 ? 4 : 6;
     return c;
 }
 

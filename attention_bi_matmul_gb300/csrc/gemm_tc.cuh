@@ -207,6 +207,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                             tma_load_2d(sB + s * B_BYTES + j * 8192, &tmB, &full[s],
                                         static_cast<int32_t>(nb * BN + j * 64), kb * TC_BK);
                     }
+                    // Weight tiles a ring's depth further on start moving into L2 now, so that
+                    // a block streaming weights keeps twice the ring's bytes in flight.
+                    if (kb + STAGES < KB) {
+                        const int32_t kp = (kb + STAGES) * TC_BK;
+                        if (!B_MN) {
+                            tma_prefetch_2d(&tmB, kp, static_cast<int32_t>(nb * BN));
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < BN / 64; ++j)
+                                tma_prefetch_2d(&tmB, static_cast<int32_t>(nb * BN + j * 64), kp);
+                        }
+                    }
                 }
             }
             if (!ok) {
@@ -344,15 +356,12 @@ bi_status launch_gemm_tc_typed(const void *a, int64_t lda, const void *b, int64_
     }
     if (b_nk) {
         switch (BN) {
-            case 64: return launch_tc_inst<T, 64, false>(ta, tb, args, cfg.stages, s);
-            case 96: return launch_tc_inst<T, 96, false>(ta, tb, args, cfg.stages, s);
             case 128: return launch_tc_inst<T, 128, false>(ta, tb, args, cfg.stages, s);
             case 256: return launch_tc_inst<T, 256, false>(ta, tb, args, cfg.stages, s);
             default: return BI_ERR_UNSUPPORTED;
         }
     } else {
         switch (BN) {
-            case 64: return launch_tc_inst<T, 64, true>(ta, tb, args, cfg.stages, s);
             case 128: return launch_tc_inst<T, 128, true>(ta, tb, args, cfg.stages, s);
             case 256: return launch_tc_inst<T, 256, true>(ta, tb, args, cfg.stages, s);
             default: return BI_ERR_UNSUPPORTED;

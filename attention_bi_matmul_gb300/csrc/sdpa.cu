@@ -13,27 +13,35 @@
 //     therefore sits in the same row of the same tile for every query length;
 //   * keys are visited in chunks of 128 at absolute key positions 0,128,256,...
 //     in ascending order.  For each chunk: S = Q K^T (tcgen05.mma into tensor
-//     memory), one thread per row applies the causal mask (key j visible iff
-//     j <= position), m' = max(m, max_j s_j*scale*log2 e),  alpha = 2^(m - m'),
-//     p_j = 2^(s_j*scale*log2 e - m'), l = l*alpha + sum_j p_j (sequential j),
-//     P rounded to the input dtype, O_chunk = P V (tcgen05.mma), and
-//     acc = fma(acc, alpha, O_chunk) in fp32 registers;
+//     memory); the causal mask (key j visible iff j <= position);
+//     m' = max(m, (max of the visible s_j) * c) with c = scale * log2 e;
+//     alpha = 2^(m - m');  p_j = 2^(fma(s_j, c, -m'));  l = l * alpha + (half
+//     sum over keys 0..63 + half sum over keys 64..127), each half summed as
+//     four interleaved partial sums (key mod 4) added as (0+1)+(2+3);  P rounded
+//     to the input dtype;  O_chunk = P V (tcgen05.mma);  acc = fma(acc, alpha,
+//     O_chunk) in fp32 registers.  2^x is the hardware's ex2.approx.ftz.f32;
 //   * a chunk that is entirely masked for a row leaves m, l and acc bit-for-bit
-//     unchanged (alpha = 2^0 = 1, p = 0), so extra chunks that a longer query
-//     tile visits, or keys appended beyond a token, change none of its bits;
+//     unchanged (alpha = 1, p = 0), so extra chunks that a longer query tile
+//     visits, or keys appended beyond a token, change none of its bits;
 //   * o = acc / l (IEEE division), rounded once to the output dtype.
+// Every quantity of a row depends only on that row's query, the keys/values,
+// the chunk positions and the row's absolute position -- never on which other
+// rows share the tile.
 //
-// Roles (448 threads):
-//   warp 0 lane 0   TMA producer (Q once; K and V chunks through 2-deep rings)
+// Roles (320 threads):
+//   warp 0 lane 0   TMA producer (Q once; K and V chunks through 2-deep rings,
+//                   plus L2 prefetch of the next chunks)
 //   warp 1          TMEM allocation (512 columns); lane 0 issues the MMAs
-//   warps 2..5      softmax: one thread per row, S from TMEM, P to shared memory
-//   warps 6..13     correction: one thread per (row, half of the head dim), O
-//                   chunks from TMEM into the fp32 accumulator, final
-//                   normalisation and store
+//   warps 2..9      row warps: warp w serves tile rows 32*(w%4)..+31 (its TMEM
+//                   lane quarter) and key/head-dim half (w-2)/4: softmax of its
+//                   64 score columns, P for that half, and the fp32
+//                   accumulator of its 64 output columns.  The two warps of a
+//                   row exchange the chunk maximum and the half sums through
+//                   shared memory (named barrier per lane quarter).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
-#include "gemm_tc.cuh"  // to_f32 / from_f32 / IsBf16
+#include "gemm_tc.cuh"  // to_f32 / from_f32 / IsBf16 / pack8
 #include "internal.cuh"
 #include "ptx.cuh"
 
@@ -46,7 +54,8 @@ constexpr int SD_C = 128;       // keys per chunk
 constexpr int SD_ROWS = 128;    // rows per query tile
 constexpr int SD_KST = 2;       // K ring depth
 constexpr int SD_VST = 2;       // V ring depth
-constexpr int SD_THREADS = 448;
+constexpr int SD_PF = 2;        // chunks prefetched into L2 beyond the rings
+constexpr int SD_THREADS = 320;
 constexpr uint32_t SD_PANEL = SD_ROWS * 128;        // 16 KB: 128 rows x 64 elements
 constexpr uint32_t SD_TILE = 2 * SD_PANEL;          // 32 KB: 128 rows x 128 elements
 constexpr uint32_t SD_TMEM_COLS = 512;              // S0 S1 O0 O1, 128 columns each
@@ -57,15 +66,52 @@ struct SdSmem {
     static constexpr uint32_t K = Q + SD_TILE;
     static constexpr uint32_t V = K + SD_KST * SD_TILE;
     static constexpr uint32_t P = V + SD_VST * SD_TILE;
-    static constexpr uint32_t ALPHA = P + SD_TILE;              // float[2][128]
-    static constexpr uint32_t LFIN = ALPHA + 2 * 128 * 4;        // float[128]
-    static constexpr uint32_t BARS = LFIN + 128 * 4;             // uint64 barriers
-    static constexpr uint32_t NBARS = 1 + 2 * SD_KST + 2 * SD_VST + 4 + 2 + 4 + 4 + 1 + 1;
+    static constexpr uint32_t MX = P + SD_TILE;                  // float[2][128] half maxima
+    static constexpr uint32_t LS = MX + 2 * 128 * 4;             // float[2][128] half sums
+    static constexpr uint32_t BARS = LS + 2 * 128 * 4;           // uint64 barriers
+    static constexpr uint32_t NBARS = 1 + 2 * SD_KST + 2 * SD_VST + 4 + 2 + 4 + 1;
     static constexpr uint32_t MISC = BARS + NBARS * 8;           // tmem slot, abort flag
     static constexpr uint32_t END = MISC + 16;
 };
 constexpr size_t SD_SMEM_BYTES = 1024 + SdSmem::END;
 
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// 8 fp32 -> 8 x 16-bit (16 bytes), converted two at a time (round to nearest even).
+template <typename T> __device__ __forceinline__ uint32_t cvt2(float a, float b);
+template <> __device__ __forceinline__ uint32_t cvt2<__nv_bfloat16>(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+template <> __device__ __forceinline__ uint32_t cvt2<__half>(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+template <typename T>
+__device__ __forceinline__ uint4 pack8x2(const float *v) {
+    return make_uint4(cvt2<T>(v[0], v[1]), cvt2<T>(v[2], v[3]), cvt2<T>(v[4], v[5]),
+                      cvt2<T>(v[6], v[7]));
+}
+
+// Named barrier shared by the two row warps of one TMEM lane quarter.
+__device__ __forceinline__ void pair_sync(uint32_t quarter) {
+    asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap *m, int32_t c0, int32_t c1,
+                                                int32_t c2, int32_t c3) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+
+// Registers are granted to warps in groups of four, so a 10-warp block is
+// budgeted as 12 warps: at most 168 registers per thread.
 template <typename T>
 __global__ void __launch_bounds__(SD_THREADS, 1)
     sdpa_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -80,8 +126,8 @@ __global__ void __launch_bounds__(SD_THREADS, 1)
     uint8_t *sK = smem + SdSmem::K;
     uint8_t *sV = smem + SdSmem::V;
     uint8_t *sP = smem + SdSmem::P;
-    float *alpha_s = reinterpret_cast<float *>(smem + SdSmem::ALPHA);
-    float *lfin_s = reinterpret_cast<float *>(smem + SdSmem::LFIN);
+    float *mx_s = reinterpret_cast<float *>(smem + SdSmem::MX);
+    float *ls_s = reinterpret_cast<float *>(smem + SdSmem::LS);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + SdSmem::BARS);
     uint64_t *bar_q = bars;
     uint64_t *kfull = bar_q + 1;
@@ -94,10 +140,7 @@ __global__ void __launch_bounds__(SD_THREADS, 1)
     uint64_t *pempty = pfull + 1;        // [1]
     uint64_t *ofull = pempty + 1;        // [2]
     uint64_t *oempty = ofull + 2;        // [2]
-    uint64_t *afull = oempty + 2;        // [2]
-    uint64_t *aempty = afull + 2;        // [2]
-    uint64_t *lfull = aempty + 2;        // [1]
-    uint64_t *mma_done = lfull + 1;      // [1]
+    uint64_t *mma_done = oempty + 2;     // [1]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + SdSmem::MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SdSmem::MISC + 4);
 
@@ -109,7 +152,6 @@ __global__ void __launch_bounds__(SD_THREADS, 1)
     const int64_t q_offset = args.q_offset;
     const int64_t Lq = args.Lq, Lkv = args.Lkv;
     // Query tiles of this call, heaviest (latest positions) first.
-    const int64_t t_first = q_offset / Qt;
     const int64_t t_last = (q_offset + Lq - 1) / Qt;
     const int64_t tile = t_last - static_cast<int64_t>(blockIdx.x);
     const int kvh = static_cast<int>(blockIdx.y);
@@ -119,7 +161,6 @@ __global__ void __launch_bounds__(SD_THREADS, 1)
     if (p_max > q_offset + Lq - 1) p_max = q_offset + Lq - 1;
     const int nchunks = args.causal ? static_cast<int>(p_max / SD_C + 1)
                                     : static_cast<int>((Lkv + SD_C - 1) / SD_C);
-    (void)t_first;
 
     if (threadIdx.x == 0) {
         mbar_init(bar_q, 1);
@@ -127,15 +168,12 @@ __global__ void __launch_bounds__(SD_THREADS, 1)
         for (int s = 0; s < SD_VST; ++s) { mbar_init(&vfull[s], 1); mbar_init(&vempty[s], 1); }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sfull[i], 1);
-            mbar_init(&sempty[i], 4);
+            mbar_init(&sempty[i], 8);
             mbar_init(&ofull[i], 1);
             mbar_init(&oempty[i], 8);
-            mbar_init(&afull[i], 4);
-            mbar_init(&aempty[i], 8);
         }
-        mbar_init(pfull, 4);
+        mbar_init(pfull, 8);
         mbar_init(pempty, 1);
-        mbar_init(lfull, 4);
         mbar_init(mma_done, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -159,6 +197,12 @@ __global__ void __launch_bounds__(SD_THREADS, 1)
             mbar_arrive_expect_tx(bar_q, SD_TILE);
             tma_load_4d(sQ, &tmQ, bar_q, 0, kvh * G, qi0, b);
             tma_load_4d(sQ + SD_PANEL, &tmQ, bar_q, 64, kvh * G, qi0, b);
+            for (int j = SD_KST; j < SD_KST + SD_PF && j < nchunks; ++j) {
+                tma_prefetch_4d(&tmK, 0, j * SD_C, kvh, b);
+                tma_prefetch_4d(&tmK, 64, j * SD_C, kvh, b);
+                tma_prefetch_4d(&tmV, 0, j * SD_C, kvh, b);
+                tma_prefetch_4d(&tmV, 64, j * SD_C, kvh, b);
+            }
             int armed = 0;
             bool ok = true;
             for (int j = 0; j < nchunks; ++j) {
@@ -173,6 +217,13 @@ __global__ void __launch_bounds__(SD_THREADS, 1)
                 tma_load_4d(sV + sv * SD_TILE, &tmV, &vfull[sv], 0, j * SD_C, kvh, b);
                 tma_load_4d(sV + sv * SD_TILE + SD_PANEL, &tmV, &vfull[sv], 64, j * SD_C, kvh, b);
                 armed = 2 * j + 2;
+                const int jp = j + SD_KST + SD_PF;   // next chunk not yet asked for
+                if (jp < nchunks) {
+                    tma_prefetch_4d(&tmK, 0, jp * SD_C, kvh, b);
+                    tma_prefetch_4d(&tmK, 64, jp * SD_C, kvh, b);
+                    tma_prefetch_4d(&tmV, 0, jp * SD_C, kvh, b);
+                    tma_prefetch_4d(&tmV, 64, jp * SD_C, kvh, b);
+                }
             }
             if (!ok) {
                 // Let every copy already issued land before the block can exit.
@@ -234,139 +285,139 @@ __global__ void __launch_bounds__(SD_THREADS, 1)
             mbar_wait_limited(mma_done, 0, WAIT_LIMIT_NS);
         }
     } else {
+        // ------------------------------------------------ row warps (2..9)
+        // These warps never leave the chunk loop early: a failed wait (the CTA is
+        // aborting) only turns the remaining work into no-ops, so the two warps of
+        // a lane quarter always meet at the same named barriers.
         const uint32_t quarter = static_cast<uint32_t>(warp & 3);
-        const int r = static_cast<int>(quarter) * 32 + lane;   // tile row == TMEM lane
+        const int half = (warp - 2) >> 2;                    // 0: keys/dims 0..63, 1: 64..127
+        const int r = static_cast<int>(quarter) * 32 + lane; // tile row == TMEM lane
         const int qi = r / G, g = r - (r / G) * G;
         const int64_t pos = p_lo + qi;
         const bool valid = pos >= q_offset && pos < q_offset + Lq;
         const bool warp_valid = __any_sync(0xffffffffu, valid) != 0;
         const uint32_t lane_base = (quarter * 32u) << 16;
+        const float sl2 = args.scale_log2;
+        // Keys [0, vis_end) are visible to this row.  Rows of the tile that hold no
+        // query of this call compute as if every key were visible; their results
+        // stay in their own rows and are never stored.
+        int64_t vis_end = args.causal ? pos + 1 : Lkv;
+        if (vis_end > Lkv) vis_end = Lkv;
+        if (!valid) vis_end = INT64_MAX / 2;
 
-        if (warp < 6) {
-            // ------------------------------------------------ softmax (warps 2..5)
-            const float sl2 = args.scale_log2;
-            float m_run = -INFINITY, l_run = 0.0f;
-            int64_t vis_end = args.causal ? pos + 1 : Lkv;   // keys [0, vis_end) visible
-            if (vis_end > Lkv) vis_end = Lkv;
-            for (int j = 0; j < nchunks; ++j) {
+        float acc[64];
+#pragma unroll
+        for (int d = 0; d < 64; ++d) acc[d] = 0.0f;
+        float m_run = -INFINITY, l_run = 0.0f, alpha_prev = 1.0f;
+
+        for (int j = 0; j <= nchunks; ++j) {
+            float alpha = 1.0f;
+            if (j < nchunks) {
+                // ---------------- softmax of chunk j over this half's 64 keys
                 const uint32_t sb = j & 1;
-                if (!warp_wait(&sfull[sb], (j >> 1) & 1u, abort_flag)) break;
+                warp_wait(&sfull[sb], (j >> 1) & 1u, abort_flag);
                 tc_fence_after();
-                int64_t lim64 = valid ? vis_end - static_cast<int64_t>(j) * SD_C : 0;
-                const int lim = lim64 < 0 ? 0 : (lim64 > SD_C ? SD_C : static_cast<int>(lim64));
-                const uint32_t s_addr = tmem_base + lane_base + sb * 128;
-                float alpha = 1.0f;
-                float m_new = m_run;
+                const int64_t lim64 = vis_end - static_cast<int64_t>(j) * SD_C - half * 64;
+                const int lim = lim64 < 0 ? 0 : (lim64 > 64 ? 64 : static_cast<int>(lim64));
+                const bool full = __all_sync(0xffffffffu, lim == 64) != 0;
+                float x[64];
+                float mloc = -INFINITY;
                 if (warp_valid) {
-                    // pass 1: running maximum of the scaled visible scores, c = 0..127
-                    float mloc = -INFINITY;
-#pragma unroll 1
-                    for (int c4 = 0; c4 < 4; ++c4) {
-                        uint32_t sr[32];
-                        tmem_ld32(s_addr + c4 * 32, sr);
-                        tmem_wait_ld(sr);
+                    uint32_t(&x0)[32] = *reinterpret_cast<uint32_t(*)[32]>(x);
+                    uint32_t(&x1)[32] = *reinterpret_cast<uint32_t(*)[32]>(x + 32);
+                    const uint32_t s_addr = tmem_base + lane_base + sb * 128 + half * 64;
+                    tmem_ld32(s_addr, x0);
+                    tmem_ld32(s_addr + 32, x1);
+                    tmem_wait_ld(x0);
+                    tmem_wait_ld(x1);
+                    // Raw-score maximum of the visible keys; scaling by sl2 > 0 after the
+                    // maximum gives exactly the maximum of the scaled scores.
+                    if (full) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const int c = c4 * 32 + i;
-                            const float x = c < lim ? __fmul_rn(__uint_as_float(sr[i]), sl2) : -INFINITY;
-                            mloc = fmaxf(mloc, x);
-                        }
+                        for (int i = 0; i < 64; ++i) mloc = fmaxf(mloc, x[i]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 64; ++i)
+                            if (i < lim) mloc = fmaxf(mloc, x[i]);
                     }
-                    m_new = fmaxf(m_run, mloc);
-                    if (lim > 0) alpha = exp2f(__fsub_rn(m_run, m_new));
                 }
-                // P_j -> shared memory (K-major, 128-byte swizzle), after PV(j-1) has read P_{j-1}
-                if (!warp_wait(pempty, (j & 1u) ^ 1u, abort_flag)) break;
+                // S(j) is in registers: release its TMEM buffer for S(j+2).
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sempty[sb]);
+                mx_s[half * 128 + r] = mloc;
+                pair_sync(quarter);
+                const float mraw = fmaxf(mx_s[r], mx_s[128 + r]);
+                const bool any = mraw != -INFINITY;                 // some key of the chunk visible
+                const float m_new = any ? fmaxf(m_run, __fmul_rn(mraw, sl2)) : m_run;
+                if (any) alpha = ex2_approx(__fsub_rn(m_run, m_new));
+                // p = 2^(s * sl2 - m') for the visible keys, 0 for the others
+                float ls4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
                 if (warp_valid) {
-                    // pass 2: p = 2^(x - m'), running sum in c order, P rounded to T
-                    float lsum = 0.0f;
-#pragma unroll 1
-                    for (int c4 = 0; c4 < 4; ++c4) {
-                        uint32_t sr[32];
-                        tmem_ld32(s_addr + c4 * 32, sr);
-                        tmem_wait_ld(sr);
-                        float pv[32];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const int c = c4 * 32 + i;
-                            float e = 0.0f;
-                            if (c < lim)
-                                e = exp2f(__fsub_rn(__fmul_rn(__uint_as_float(sr[i]), sl2), m_new));
-                            pv[i] = e;
-                            lsum = __fadd_rn(lsum, e);
-                        }
-#pragma unroll
-                        for (int q8 = 0; q8 < 4; ++q8) {
-                            const int cc = (c4 & 1) * 4 + q8;        // 16-byte chunk in the panel
-                            const uint4 v = pack8<T>(pv + q8 * 8);
-                            uint8_t *dst = sP + (c4 >> 1) * SD_PANEL + r * 128 + ((cc ^ (r & 7)) << 4);
-                            *reinterpret_cast<uint4 *>(dst) = v;
-                        }
+                    for (int i = 0; i < 64; ++i) {
+                        float e = ex2_approx(__fmaf_rn(x[i], sl2, -m_new));
+                        if (!full && i >= lim) e = 0.0f;
+                        x[i] = e;
+                        ls4[i & 3] = __fadd_rn(ls4[i & 3], e);
                     }
-                    if (lim > 0) {
-                        l_run = __fadd_rn(__fmul_rn(l_run, alpha), lsum);
-                        m_run = m_new;
+                }
+                const float lsum = __fadd_rn(__fadd_rn(ls4[0], ls4[1]), __fadd_rn(ls4[2], ls4[3]));
+                // P_j -> shared memory (panel `half`), once PV(j-1) has read P_{j-1}
+                warp_wait(pempty, (j & 1u) ^ 1u, abort_flag);
+                if (warp_valid) {
+#pragma unroll
+                    for (int cc = 0; cc < 8; ++cc) {
+                        const uint4 v = pack8x2<T>(x + cc * 8);
+                        uint8_t *dst = sP + half * SD_PANEL + r * 128 + ((cc ^ (r & 7)) << 4);
+                        *reinterpret_cast<uint4 *>(dst) = v;
                     }
                     fence_proxy_async_smem();
                 }
-                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&sempty[sb]);
-                    mbar_arrive(pfull);
+                if (lane == 0) mbar_arrive(pfull);
+                ls_s[half * 128 + r] = lsum;
+                pair_sync(quarter);
+                if (any) {
+                    l_run = __fadd_rn(__fmul_rn(l_run, alpha), __fadd_rn(ls_s[r], ls_s[128 + r]));
+                    m_run = m_new;
                 }
-                // alpha_j -> correction warps
-                if (!warp_wait(&aempty[sb], ((j >> 1) & 1u) ^ 1u, abort_flag)) break;
-                alpha_s[sb * 128 + r] = alpha;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&afull[sb]);
             }
-            lfin_s[r] = l_run;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(lfull);
-        } else {
-            // ------------------------------------------------ correction (warps 6..13)
-            constexpr int HD = SD_D / 2;                    // head-dim columns per thread
-            const int col0 = ((warp - 6) >> 2) * HD;        // 0 or 64
-            float acc[HD];
-#pragma unroll
-            for (int d = 0; d < HD; ++d) acc[d] = 0.0f;
-            bool ok = true;
-            for (int j = 0; j < nchunks; ++j) {
-                const uint32_t ob = j & 1;
-                if (!warp_wait(&afull[ob], (j >> 1) & 1u, abort_flag)) { ok = false; break; }
-                const float alpha = alpha_s[ob * 128 + r];
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&aempty[ob]);
-                if (!warp_wait(&ofull[ob], (j >> 1) & 1u, abort_flag)) { ok = false; break; }
+            if (j >= 1) {
+                // ---------------- accumulate O of chunk j-1 (its alpha was computed last round)
+                const int i = j - 1;
+                const uint32_t ob = i & 1;
+                warp_wait(&ofull[ob], (i >> 1) & 1u, abort_flag);
                 tc_fence_after();
                 if (warp_valid) {
+                    uint32_t o0[32], o1[32];
+                    const uint32_t o_addr = tmem_base + lane_base + 256 + ob * 128 + half * 64;
+                    tmem_ld32(o_addr, o0);
+                    tmem_ld32(o_addr + 32, o1);
+                    tmem_wait_ld(o0);
+                    tmem_wait_ld(o1);
 #pragma unroll
-                    for (int c = 0; c < HD / 32; ++c) {
-                        uint32_t o[32];
-                        tmem_ld32(tmem_base + lane_base + 256 + ob * 128 + col0 + c * 32, o);
-                        tmem_wait_ld(o);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            acc[c * 32 + i] = __fmaf_rn(acc[c * 32 + i], alpha, __uint_as_float(o[i]));
+                    for (int e = 0; e < 32; ++e) {
+                        acc[e] = __fmaf_rn(acc[e], alpha_prev, __uint_as_float(o0[e]));
+                        acc[32 + e] = __fmaf_rn(acc[32 + e], alpha_prev, __uint_as_float(o1[e]));
                     }
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&oempty[ob]);
             }
-            if (ok && warp_wait(lfull, 0, abort_flag) && valid) {
-                const float l = lfin_s[r];
-                const int h = kvh * G + g;
-                T *orow = static_cast<T *>(args.o) + b * args.os[0] + h * args.os[1] +
-                          (pos - q_offset) * args.os[2] + col0;
+            alpha_prev = alpha;
+        }
+        if (valid && !*abort_flag) {
+            const int h = kvh * G + g;
+            T *orow = static_cast<T *>(args.o) + b * args.os[0] + h * args.os[1] +
+                      (pos - q_offset) * args.os[2] + half * 64;
 #pragma unroll
-                for (int d8 = 0; d8 < HD / 8; ++d8) {
-                    float v[8];
+            for (int d8 = 0; d8 < 8; ++d8) {
+                float v[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) v[i] = __fdiv_rn(acc[d8 * 8 + i], l);
-                    *reinterpret_cast<uint4 *>(orow + d8 * 8) = pack8<T>(v);
-                }
+                for (int e = 0; e < 8; ++e) v[e] = __fdiv_rn(acc[d8 * 8 + e], l_run);
+                *reinterpret_cast<uint4 *>(orow + d8 * 8) = pack8<T>(v);
             }
         }
     }

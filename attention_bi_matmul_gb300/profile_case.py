@@ -1,0 +1,63 @@
+"""Run one kernel case a few times, for profilers (ncu) and quick timing.
+
+  python -m attention_bi_matmul_gb300.profile_case linear M N K [--reps R]
+  python -m attention_bi_matmul_gb300.profile_case matmul M N K [--reps R]
+  python -m attention_bi_matmul_gb300.profile_case sdpa B H Hkv Lq Lkv [--reps R]
+
+Inputs are seeded synthetic bf16 tensors on cuda:0.  Prints the CUDA-event
+time per call of the last repetitions (not meaningful under a profiler).
+"""
+from __future__ import annotations
+
+import argparse
+import math
+import os
+import sys
+
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("op", choices=("linear", "matmul", "sdpa"))
+    ap.add_argument("dims", type=int, nargs="+")
+    ap.add_argument("--reps", type=int, default=3)
+    args = ap.parse_args()
+
+    import attention_bi_matmul_gb300 as bi
+    from attention_bi_matmul_gb300 import synth
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    if args.op in ("linear", "matmul"):
+        M, N, K = args.dims
+        a, b = synth.gemm16(M, N, K, "bf16", seed=0, layout=args.op, device=dev)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        fn = (lambda: bi.linear(a, b, out=y)) if args.op == "linear" else (lambda: bi.matmul(a, b, out=y))
+        work = "%.3f GFLOP" % (2.0 * M * N * K / 1e9)
+    else:
+        B, H, Hkv, Lq, Lkv = args.dims
+        q, k, v = synth.sdpa_qkv(B, H, Hkv, Lq, Lkv, 128, "bf16", seed=0, device=dev)
+        o = torch.empty_like(q)
+        fn = lambda: bi.sdpa(q, k, v, causal=True, out=o)
+        work = "%.3f GB of K/V" % (4.0 * B * Hkv * Lkv * 128 / 1e9)
+    fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.reps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    st, code = bi.last_device_error()
+    print("%s %s: %s, %.4f ms per call, device status %d" % (
+        args.op, args.dims, work, e0.elapsed_time(e1) / args.reps, st))
+    if st != 0:
+        sys.exit(1)
+
+
+if __name__ == "__main__":
+    main()

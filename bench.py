@@ -1,0 +1,527 @@
+#!/usr/bin/env python
+"""Throughput of the batch-invariant hot path on GB300, one JSON line.
+
+One step = one pass of the whole path over synthetic bf16 inputs resident in HBM:
+  1. batch sweep    bi_linear, K=4096, N in {4096, 11008, 14336},
+                    M in {1,2,3,4,8,16,32,64,128,256,512}; every call reads a
+                    different one of 4 weight copies per N (960 MB > L2), as a
+                    decode step streams each layer's weight once;
+  2. large GEMM     bi_linear, M = N = K = 8192;
+  3. decode SDPA    bi_sdpa, B=32, H=32, Hkv=8, D=128, KV length 32768, causal;
+  4. decoder glue   embedding, RMSNorm, RoPE, SwiGLU and residual add at the
+                    decoder's shapes (d=2048, 16/4 heads, MLP 5632) for 8 x 128
+                    prompt tokens.
+value = algorithmic FLOPs of the step / step time (TFLOP/s).  Per-part times,
+GB/s and roofline fractions are reported under "parts"; "roofline" is the
+part with the largest share of the step time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload (rank 0 only).  Under torchrun each rank runs an independent replica
+on its own GPU (the path has no cross-GPU exchange); value sums all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "bf16 GEMM TFLOP/s & SDPA GB/s vs roofline at batch 1–512; 0 bits differing"
+C2_N = (4096, 11008, 14336)
+C2_M = (1, 2, 3, 4, 8, 16, 32, 64, 128, 256, 512)
+C2_K = 4096
+WCOPIES = 4
+BIG = 8192
+SD = dict(B=32, H=32, Hkv=8, D=128, L=32768)
+DEC = dict(B=8, L=128, d=2048, H=16, Hkv=4, D=128, I=5632, V=32000)
+
+CONFIG = {
+    "workload": "throughput sweep: bf16 linear K=4096 N{4096,11008,14336} M{1..512} (4 rotating "
+                "weight copies) + bf16 linear 8192^3 + causal GQA decode SDPA B32 H32 Hkv8 D128 "
+                "KV32768 + decoder glue (d2048, 8x128 tokens)",
+    "dtype": "bf16",
+    "batch_sweep": list(C2_M),
+    "l2": "inputs larger than L2 (rotating weight copies; 4.3 GB KV cache; 128 MB GEMM operands)",
+}
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ------------------------------------------------------------------ work accounting
+
+def step_flops():
+    c2 = sum(2.0 * M * N * C2_K for N in C2_N for M in C2_M)
+    big = 2.0 * BIG ** 3
+    sd = 4.0 * SD["B"] * SD["H"] * SD["D"] * SD["L"]
+    return {"batch_sweep": c2, "gemm_8192": big, "sdpa_decode": sd, "glue": 0.0}
+
+
+def step_bytes():
+    c2 = sum(2.0 * (N * C2_K + M * C2_K + M * N) for N in C2_N for M in C2_M)
+    big = 2.0 * 3 * BIG * BIG
+    kv = 2.0 * 2 * SD["B"] * SD["Hkv"] * SD["L"] * SD["D"]
+    qo = 2.0 * 2 * SD["B"] * SD["H"] * SD["D"]
+    T = DEC["B"] * DEC["L"]
+    d, I = DEC["d"], DEC["I"]
+    glue = 2.0 * (T * d                      # embedding gather (write)
+                  + T * d + T * d            # embedding rows read + rmsnorm read
+                  + T * d + d                # rmsnorm write + weight
+                  + 2 * T * (DEC["H"] + DEC["Hkv"]) * DEC["D"]   # rope read + write
+                  + T * 2 * I + T * I        # swiglu
+                  + 3 * T * d)               # residual add
+    return {"batch_sweep": c2, "gemm_8192": big, "sdpa_decode": kv + qo, "glue": glue}
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.lines = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        rows = []
+        for (t, line) in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                rows.append((t, float(parts[2]), float(parts[3]), parts[6:10]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 <= r[0] <= t1 + 0.1]
+        use = inside if inside else rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i, v in enumerate(r[3]) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(inside), "samples_outside_window": len(use) - len(inside)}
+
+
+# ------------------------------------------------------------------ our arm
+
+class Workload:
+    def __init__(self, dev, seed: int = 0):
+        import torch
+        from attention_bi_matmul_gb300 import synth
+        bf = torch.bfloat16
+        s = 1.0 / math.sqrt(C2_K)
+        self.x = synth.normal((max(C2_M), C2_K), seed, s, bf, dev)
+        self.w = {N: [synth.normal((N, C2_K), seed + 10 * N + i, s, bf, dev) for i in range(WCOPIES)]
+                  for N in C2_N}
+        self.y = {N: torch.empty((max(C2_M), N), dtype=bf, device=dev) for N in C2_N}
+        sb = 1.0 / math.sqrt(BIG)
+        self.X = synth.normal((BIG, BIG), seed + 1, sb, bf, dev)
+        self.W = synth.normal((BIG, BIG), seed + 2, sb, bf, dev)
+        self.Y = torch.empty((BIG, BIG), dtype=bf, device=dev)
+        B, H, Hkv, D, L = SD["B"], SD["H"], SD["Hkv"], SD["D"], SD["L"]
+        self.q = synth.normal((B, H, 1, D), seed + 3, 1.0, bf, dev)
+        self.k = synth.normal((B, Hkv, L, D), seed + 4, 1.0, bf, dev)
+        self.v = synth.normal((B, Hkv, L, D), seed + 5, 1.0, bf, dev)
+        self.o = torch.empty((B, H, 1, D), dtype=bf, device=dev)
+        T, d = DEC["B"] * DEC["L"], DEC["d"]
+        self.ids = synth.uniform_ids((T,), DEC["V"], seed + 6, dev)
+        self.emb = synth.normal((DEC["V"], d), seed + 7, 0.02, bf, dev)
+        self.nw = torch.ones((d,), dtype=bf, device=dev)
+        self.h = torch.empty((T, d), dtype=bf, device=dev)
+        self.hn = torch.empty((T, d), dtype=bf, device=dev)
+        self.qr = synth.normal((DEC["B"], DEC["L"], DEC["H"] + DEC["Hkv"], DEC["D"]), seed + 8, 1.0, bf, dev)
+        self.qro = torch.empty_like(self.qr)
+        self.gu = synth.normal((T, 2 * DEC["I"]), seed + 9, 1.0, bf, dev)
+        self.act = torch.empty((T, DEC["I"]), dtype=bf, device=dev)
+        self.res = torch.empty((T, d), dtype=bf, device=dev)
+
+    def part_batch_sweep(self, bi):
+        i = 0
+        for N in C2_N:
+            for M in C2_M:
+                bi.linear(self.x[:M], self.w[N][i % WCOPIES], out=self.y[N][:M])
+                i += 1
+
+    def part_gemm(self, bi):
+        bi.linear(self.X, self.W, out=self.Y)
+
+    def part_sdpa(self, bi):
+        bi.sdpa(self.q, self.k, self.v, causal=True, out=self.o)
+
+    def part_glue(self, bi):
+        bi.embedding(self.ids, self.emb, out=self.h)
+        bi.rmsnorm(self.h, self.nw, 1e-6, out=self.hn)
+        bi.rope(self.qr, 0, out=self.qro)
+        bi.swiglu(self.gu, out=self.act)
+        bi.add(self.h, self.hn, out=self.res)
+
+    PARTS = ("batch_sweep", "gemm_8192", "sdpa_decode", "glue")
+
+    def run_parts(self, bi):
+        return [self.part_batch_sweep, self.part_gemm, self.part_sdpa, self.part_glue]
+
+
+def e2e_step(bi, host, dev):
+    """The same step through the public API with pinned host buffers: copy this step's inputs
+    host->device, run, copy the results device->host."""
+    import torch
+    x = host["x"].to(dev, non_blocking=True)
+    ws = {N: host["w"][N].to(dev, non_blocking=True) for N in C2_N}
+    X = host["X"].to(dev, non_blocking=True)
+    W = host["W"].to(dev, non_blocking=True)
+    q = host["q"].to(dev, non_blocking=True)
+    k = host["k"].to(dev, non_blocking=True)
+    v = host["v"].to(dev, non_blocking=True)
+    outs = []
+    for N in C2_N:
+        for M in C2_M:
+            outs.append((bi.linear(x[:M], ws[N]), M, N))
+    Y = bi.linear(X, W)
+    o = bi.sdpa(q, k, v, causal=True)
+    host["Y"].copy_(Y, non_blocking=True)
+    host["o"].copy_(o, non_blocking=True)
+    for (y, M, N) in outs:
+        host["ys"][N][:M].copy_(y, non_blocking=True)
+    torch.cuda.current_stream().synchronize()
+
+
+def cpu_baseline_sample(W_host, X_host, xs_host, w_host, q_host, k_host, v_host, budget_s: float):
+    """Time the fp64 oracle on a bounded sample of the step: rows of the 8192^3 GEMM, one row
+    of each batch-sweep GEMM, and one KV group (4 query heads, 32768 keys) of the decode
+    attention.  Returns (flops, seconds, rows)."""
+    import oracle
+    Wd = oracle._f64(W_host)
+    wds = {N: oracle._f64(w_host[N]) for N in C2_N}
+    x1 = oracle._f64(xs_host[:1])
+    qd = oracle._f64(q_host[0:1, 0:4])
+    kd = oracle._f64(k_host[0:1, 0:1])
+    vd = oracle._f64(v_host[0:1, 0:1])
+    fixed_flops = sum(2.0 * N * C2_K for N in C2_N) + 4.0 * 4 * SD["D"] * SD["L"]
+    t = time.perf_counter()
+    for N in C2_N:
+        oracle.linear(x1, wds[N])
+    oracle.sdpa(qd, kd, vd, causal=True)
+    t_fixed = time.perf_counter() - t
+    # calibrate the GEMM row rate, then fill the remaining budget
+    R0 = 16
+    Xr = oracle._f64(X_host[:R0])
+    t = time.perf_counter()
+    oracle.linear(Xr, Wd)
+    t_r0 = time.perf_counter() - t
+    R = int(max(R0, min(BIG, R0 * max(budget_s - t_fixed, 0.1) / max(t_r0, 1e-6))))
+    Xr = oracle._f64(X_host[:R])
+    t = time.perf_counter()
+    oracle.linear(Xr, Wd)
+    t_rows = time.perf_counter() - t
+    flops = fixed_flops + 2.0 * R * BIG * BIG
+    return flops, t_fixed + t_rows, R
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+    import attention_bi_matmul_gb300 as bi
+
+    hbm, tf_burst, tf_sust, peak_src = load_peaks()
+    wl = Workload(dev)
+    parts = wl.run_parts(bi)
+    torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        for p in parts:
+            p(bi)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(parts) + 1)] for _ in range(K)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    # keep the GPU busy while the sampler starts, so its first samples see the loaded clock
+    t_pre = time.time()
+    while time.time() - t_pre < 0.4:
+        for p in parts:
+            p(bi)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = bi.launch_count()
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    start.record()
+    for s in range(K):
+        ev[s][0].record()
+        for i, p in enumerate(parts):
+            p(bi)
+            ev[s][i + 1].record()
+    stop.record()
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    launches = bi.launch_count() - launches0
+    if world > 1:
+        dist.barrier()
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1)
+
+    ms_total = start.elapsed_time(stop)
+    part_ms = [sum(ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(K)) / K
+               for i in range(len(parts))]
+    t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_per_step = float(t.item()) / K
+
+    st, code = bi.last_device_error()
+    if st != 0:
+        raise RuntimeError("device error word %#x after the timed region" % code)
+
+    flops = step_flops()
+    byts = step_bytes()
+    step_f = sum(flops.values())
+    value = world * step_f / (ms_per_step * 1e-3) / 1e12
+
+    pinfo = {}
+    for name, ms in zip(Workload.PARTS, part_ms):
+        d = {"ms": round(ms, 4)}
+        if flops[name] > 0:
+            d["tflops"] = round(flops[name] / (ms * 1e-3) / 1e12, 2)
+        d["gbs"] = round(byts[name] / (ms * 1e-3) / 1e9, 1)
+        if name == "gemm_8192":
+            d["frac_tensor_burst"] = round(d["tflops"] / tf_burst, 4)
+            d["frac_tensor_sustained"] = round(d["tflops"] / tf_sust, 4)
+        else:
+            d["frac_hbm"] = round(d["gbs"] / hbm, 4)
+        pinfo[name] = d
+    # per-M view of the batch sweep is in the profiles; the headline roofline is the dominant part
+    dom = max(Workload.PARTS, key=lambda n: pinfo[n]["ms"])
+    traffic = load_traffic(dom)
+    if dom == "gemm_8192":
+        roof = {"bound": "tensor", "achieved": pinfo[dom]["tflops"], "peak": tf_burst,
+                "unit": "TFLOP/s", "frac": round(pinfo[dom]["tflops"] / tf_burst, 4),
+                "traffic": traffic, "kernel": "gemm_tc_kernel (bi_linear 8192^3)",
+                "peak_source": peak_src + " bf16 burst"}
+    else:
+        roof = {"bound": "hbm", "achieved": pinfo[dom]["gbs"], "peak": hbm, "unit": "GB/s",
+                "frac": round(pinfo[dom]["gbs"] / hbm, 4), "traffic": traffic,
+                "kernel": {"sdpa_decode": "sdpa_kernel (bi_sdpa decode)",
+                           "batch_sweep": "gemm_tc_kernel (bi_linear batch sweep)",
+                           "glue": "glue kernels"}[dom],
+                "peak_source": peak_src + " HBM copy"}
+
+    # ---- end to end through the public API with host buffers
+    host = {"x": wl.x.cpu().pin_memory(), "w": {N: wl.w[N][0].cpu().pin_memory() for N in C2_N},
+            "X": wl.X.cpu().pin_memory(), "W": wl.W.cpu().pin_memory(),
+            "q": wl.q.cpu().pin_memory(), "k": wl.k.cpu().pin_memory(), "v": wl.v.cpu().pin_memory(),
+            "Y": torch.empty_like(wl.Y, device="cpu").pin_memory(),
+            "o": torch.empty_like(wl.o, device="cpu").pin_memory(),
+            "ys": {N: torch.empty((max(C2_M), N), dtype=torch.bfloat16).pin_memory() for N in C2_N}}
+    h2d = sum(t.numel() * t.element_size() for t in
+              [host["x"], host["X"], host["W"], host["q"], host["k"], host["v"]] + list(host["w"].values()))
+    d2h = (host["Y"].numel() + host["o"].numel() + sum(M * N for N in C2_N for M in C2_M)) * 2
+    for _ in range(2):
+        e2e_step(bi, host, dev)
+    Ke = max(3, min(K, 20))
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(Ke):
+        e2e_step(bi, host, dev)
+    e1.record()
+    torch.cuda.synchronize()
+    te = torch.tensor([e0.elapsed_time(e1) / Ke], device=dev, dtype=torch.float64)
+    if world > 1:
+        dist.all_reduce(te, op=dist.ReduceOp.MAX)
+    e2e_val = world * step_f / (float(te.item()) * 1e-3) / 1e12
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        fl, secs, R = cpu_baseline_sample(wl.W.cpu(), wl.X.cpu(), wl.x.cpu(),
+                                          {N: wl.w[N][0].cpu() for N in C2_N},
+                                          wl.q.cpu(), wl.k.cpu(), wl.v.cpu(), budget_s=12.0)
+        cpu = {"value": fl / secs / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+               "kind": "oracle", "seconds": round(secs, 2),
+               "sample": "%d rows of the 8192^3 linear + one row of each batch-sweep linear (M=1) + "
+                         "one KV group (4 heads x 32768 keys) of the decode attention" % R}
+
+    if rank == 0:
+        out = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+               "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+               "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+               "data": "synthetic (seeded torch CUDA generator; shapes and distributions of the "
+                       "configs)",
+               "config": dict(CONFIG, parallelism="replicas x%d" % world),
+               "roofline": roof, "parts": pinfo, "cpu_baseline": cpu,
+               "e2e": {"value": round(e2e_val, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                       "d2h_bytes_per_step": d2h},
+               "gpu_launches": launches, "clocks": clocks}
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def load_traffic(part: str):
+    """DRAM bytes per launch from the committed ncu summary of this part's kernel, if current."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        return t.get(part)
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------ reference arm (the oracle)
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import torch
+    import oracle
+    from attention_bi_matmul_gb300 import synth
+    oracle.build()
+    bf = torch.bfloat16
+    # the same seeded inputs, drawn on the CPU only where the sample needs them
+    s = 1.0 / math.sqrt(C2_K)
+    sb = 1.0 / math.sqrt(BIG)
+    x = synth.normal((1, C2_K), 0, s, bf)
+    ws = {N: synth.normal((N, C2_K), 10 * N, s, bf) for N in C2_N}
+    X = synth.normal((64, BIG), 1, sb, bf)
+    W = synth.normal((BIG, BIG), 2, sb, bf)
+    q = synth.normal((1, 4, 1, SD["D"]), 3, 1.0, bf)
+    k = synth.normal((1, 1, SD["L"], SD["D"]), 4, 1.0, bf)
+    v = synth.normal((1, 1, SD["L"], SD["D"]), 5, 1.0, bf)
+    Wd = oracle._f64(W)
+    wds = {N: oracle._f64(ws[N]) for N in C2_N}
+    xd = oracle._f64(x)
+    qd, kd, vd = oracle._f64(q), oracle._f64(k), oracle._f64(v)
+    total = args.steps + args.warmup
+    budget = max(0.3, 150.0 / max(total, 1))   # the whole run stays within a few minutes
+    # calibrate rows of the big GEMM per step
+    t = time.perf_counter()
+    oracle.linear(oracle._f64(X[:8]), Wd)
+    t8 = time.perf_counter() - t
+    t = time.perf_counter()
+    for N in C2_N:
+        oracle.linear(xd, wds[N])
+    oracle.sdpa(qd, kd, vd, causal=True)
+    tfix = time.perf_counter() - t
+    R = int(max(1, min(64, 8 * max(budget - tfix, 0.05) / max(t8, 1e-6))))
+    Xd = oracle._f64(X[:R])
+
+    def step():
+        for N in C2_N:
+            oracle.linear(xd, wds[N])
+        oracle.sdpa(qd, kd, vd, causal=True)
+        oracle.linear(Xd, Wd)
+
+    flops = sum(2.0 * N * C2_K for N in C2_N) + 4.0 * 4 * SD["D"] * SD["L"] + 2.0 * R * BIG * BIG
+    for _ in range(args.warmup):
+        step()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    secs = (time.perf_counter() - t) / max(args.steps, 1)
+    val = flops / secs / 1e12
+    sample = ("per step: %d rows of the 8192^3 linear + one row of each batch-sweep linear (M=1) + "
+              "one KV group (4 heads x 32768 keys) of the decode attention" % R)
+    out = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs * 1e3, 3),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic (seeded torch CPU generator; shapes of the configs)",
+           "config": dict(CONFIG, parallelism="oracle on host cores"),
+           "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                            "kind": "oracle", "sample": sample},
+           "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip timing the CPU oracle (for profiling runs)")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

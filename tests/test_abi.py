@@ -39,15 +39,13 @@ def test_status_strings_and_version(lib):
 
 def test_gemm_config_ignores_M_and_is_host_only(lib):
     bn, st = ctypes.c_int(), ctypes.c_int()
-    for N in (512, 4096, 11008, 14336, 19456, 38912):
-        for layout in (0, 1):
-            assert lib.bi_gemm_config(N, 4096, L.BI_BF16, layout, ctypes.byref(bn),
-                                      ctypes.byref(st)) == L.BI_OK
-            assert bn.value in (64, 96, 128, 256) and st.value >= 4
-            if layout == 1:
-                assert bn.value % 64 == 0
-    assert lib.bi_gemm_config(14336, 4096, L.BI_BF16, 0, ctypes.byref(bn), None) == L.BI_OK
-    assert bn.value == 96
+    for N in (8, 512, 4096, 11008, 14336, 38912):
+        for K in (8, 4096, 8192, 16384):
+            for layout in (0, 1):
+                assert lib.bi_gemm_config(N, K, L.BI_BF16, layout, ctypes.byref(bn),
+                                          ctypes.byref(st)) == L.BI_OK
+                assert bn.value == (256 if K >= 8192 else 128)
+                assert st.value == (4 if bn.value == 256 else 6)
     assert lib.bi_gemm_config(0, 4096, L.BI_BF16, 0, None, None) == L.BI_ERR_INVALID_ARG
     assert lib.bi_gemm_config(64, 64, 7, 0, None, None) == L.BI_ERR_UNSUPPORTED
 

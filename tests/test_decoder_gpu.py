@@ -1,0 +1,147 @@
+"""The random-init 4-layer decoder: request 0's logits at batch 1 vs batch 8 (random
+neighbours), over a 128-token prompt and greedy decode steps, eager vs CUDA graph; the
+torch/cuBLAS control; and the logits against an fp64 oracle decoder (GPU)."""
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+from attention_bi_matmul_gb300 import synth
+from tolerances import assert_same_bits, count_bit_diffs
+
+pytestmark = pytest.mark.gpu
+
+PROMPT = 128
+STEPS = 4
+
+
+@pytest.fixture(scope="module")
+def model():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    from attention_bi_matmul_gb300.decoder import Decoder, DecoderConfig
+    return Decoder(DecoderConfig(), seed=0, device="cuda")
+
+
+@pytest.fixture(scope="module")
+def ids():
+    return synth.uniform_ids((8, PROMPT), 32000, seed=2024, device="cuda")
+
+
+def test_c4_batch1_vs_batch8_prefill_and_decode(model, ids):
+    c1 = model.new_cache(1, PROMPT + STEPS)
+    c8 = model.new_cache(8, PROMPT + STEPS)
+    l1 = model(ids[:1], c1, 0)
+    l8 = model(ids, c8, 0)
+    n = count_bit_diffs(l1[0, -1], l8[0, -1])
+    print("prefill: %d / %d logits of request 0 differ (batch 1 vs 8)" % (n, l1.shape[-1]))
+    assert n == 0
+    assert_same_bits(l1[0], l8[0], "all 128 prompt positions")
+    for t in range(STEPS):
+        n1 = l1[:, -1].argmax(-1)
+        n8 = l8[:, -1].argmax(-1)
+        assert int(n1[0]) == int(n8[0])
+        l1 = model(n1.view(1, 1), c1, PROMPT + t)
+        l8 = model(n8.view(8, 1), c8, PROMPT + t)
+        assert_same_bits(l1[0, 0], l8[0, 0], "decode step %d" % t)
+    # the KV caches of request 0 agree too
+    for (k1, v1), (k8, v8) in zip(c1, c8):
+        assert_same_bits(k1[0], k8[0], "k cache")
+        assert_same_bits(v1[0], v8[0], "v cache")
+
+
+def test_c4_eager_vs_cuda_graph(model, ids):
+    eager = model(ids, model.new_cache(8, PROMPT), 0).clone()
+    cache = model.new_cache(8, PROMPT)
+    static_ids = ids.clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        model(static_ids, cache, 0)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        out = model(static_ids, cache, 0)
+    g.replay()
+    torch.cuda.synchronize()
+    assert_same_bits(out, eager, "prefill logits, graph replay vs eager")
+    g.replay()
+    torch.cuda.synchronize()
+    assert_same_bits(out, eager, "second replay")
+
+
+def _torch_forward(model, ids, cache, pos0):
+    """The same decoder with stock torch ops (cuBLAS GEMMs, torch SDPA): the control.
+    cache: list of (k, v) [B, Hkv, Lmax, D] per layer, written at pos0.. ."""
+    c = model.cfg
+    B, L = ids.shape
+    h = model.emb[ids.reshape(-1)]
+    pos = torch.arange(pos0, pos0 + L, device=ids.device, dtype=torch.float64)
+    inv = c.rope_base ** (-2.0 * torch.arange(c.D // 2, device=ids.device, dtype=torch.float64) / c.D)
+    ang = pos[:, None] * inv[None]
+    cos, sin = ang.cos().float(), ang.sin().float()
+
+    def rope(x):  # [B, L, n, D]
+        x1, x2 = x[..., :c.D // 2].float(), x[..., c.D // 2:].float()
+        cc, ss = cos[None, :, None], sin[None, :, None]
+        return torch.cat([x1 * cc - x2 * ss, x2 * cc + x1 * ss], -1).to(x.dtype)
+
+    G = c.H // c.Hkv
+    for lw, (kc, vc) in zip(model.layers, cache):
+        n = F.rms_norm(h, (c.d,), lw["ln1"], c.eps)
+        qkv = F.linear(n, lw["wqkv"]).view(B, L, c.H + 2 * c.Hkv, c.D)
+        q = rope(qkv[:, :, :c.H]).transpose(1, 2)
+        kc[:, :, pos0:pos0 + L] = rope(qkv[:, :, c.H:c.H + c.Hkv]).transpose(1, 2)
+        vc[:, :, pos0:pos0 + L] = qkv[:, :, c.H + c.Hkv:].transpose(1, 2)
+        k = kc[:, :, :pos0 + L].repeat_interleave(G, 1)
+        v = vc[:, :, :pos0 + L].repeat_interleave(G, 1)
+        att = F.scaled_dot_product_attention(q, k, v, is_causal=(L > 1 and pos0 == 0))
+        h = h + F.linear(att.transpose(1, 2).reshape(B * L, -1), lw["wo"])
+        n = F.rms_norm(h, (c.d,), lw["ln2"], c.eps)
+        gu = F.linear(n, lw["wgu"])
+        h = h + F.linear(F.silu(gu[:, :c.inter]) * gu[:, c.inter:], lw["wdown"])
+    return F.linear(F.rms_norm(h, (c.d,), model.lnf, c.eps), model.lm_head).view(B, L, -1)
+
+
+def test_c4_torch_control(model, ids):
+    """The negative control: the same model on stock torch ops (cuBLAS, torch SDPA), request 0
+    at batch 1 vs batch 8, over the prompt and the greedy decode steps."""
+    c1 = model.new_cache(1, PROMPT + STEPS)
+    c8 = model.new_cache(8, PROMPT + STEPS)
+    l1 = _torch_forward(model, ids[:1], c1, 0)
+    l8 = _torch_forward(model, ids, c8, 0)
+    counts = [count_bit_diffs(l1[0, -1], l8[0, -1])]
+    for t in range(STEPS):
+        n1 = l1[:, -1].argmax(-1)
+        n8 = torch.cat([n1, l8[1:, -1].argmax(-1)])      # request 0 follows the same tokens
+        l1 = _torch_forward(model, n1.view(1, 1), c1, PROMPT + t)
+        l8 = _torch_forward(model, n8.view(8, 1), c8, PROMPT + t)
+        counts.append(count_bit_diffs(l1[0, 0], l8[0, 0]))
+    print("torch control: logits of request 0 differing (batch 1 vs 8), prefill then decode "
+          "steps: %s of %d" % (counts, l1.shape[-1]))
+    # The stock path is allowed to be invariant on these particular shapes (cuBLAS happened to
+    # pick the same kernels for M = 128 vs 1024 and M = 1 vs 8 on GB300); the GEMM and
+    # attention controls of the batch-size and query-length configs show that it is not in
+    # general.  This test records the measurement and checks the control ran to completion.
+    assert len(counts) == STEPS + 1 and torch.isfinite(l1).all() and torch.isfinite(l8).all()
+
+
+def test_c4_logits_match_oracle_decoder(model, ids):
+    """The GPU logits of request 0 against the fp64 oracle decoder (same bf16 storage points).
+    Per-op parity is gated elsewhere; here the gate is the end-to-end agreement: cosine
+    similarity and the share of positions whose argmax token agrees."""
+    from oracle import decoder as odec
+    c = model.cfg
+    L = 32
+    cache = model.new_cache(1, L)
+    got = model(ids[:1, :L], cache, 0)[0].double().cpu().numpy()
+    w = {"emb": model.emb, "lnf": model.lnf, "lm_head": model.lm_head, "layers": model.layers}
+    ref = odec.logits(w, ids[0, :L], c.d, c.H, c.Hkv, c.D, c.inter, c.eps, c.rope_base)
+    cos = (got * ref).sum(-1) / np.linalg.norm(got, axis=-1) / np.linalg.norm(ref, axis=-1)
+    err = np.abs(got - ref).max()
+    agree = float((got.argmax(-1) == ref.argmax(-1)).mean())
+    print("decoder vs oracle: min cosine %.6f, max |err| %.4g (logit std %.3g), argmax agree %.3f"
+          % (cos.min(), err, ref.std(), agree))
+    assert cos.min() > 0.999
+    assert agree >= 0.9

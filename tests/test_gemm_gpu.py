@@ -65,44 +65,42 @@ def test_fp32_matmul_addmm_ragged(bi, M, N, K):
 
 # ------------------------------------------------------------------ 16-bit parity, every tile width
 
-def _widths(bi):
-    """N values that select each built tile width (the width is a function of N)."""
-    out = {}
-    for layout, Ns in (("linear", (4096, 14336, 19456, 38912)), ("matmul", (4096, 19456, 38912))):
-        for N in Ns:
-            out.setdefault((layout, bi.gemm_config(N, 256, torch.bfloat16, layout)[0]), N)
-    return out
+def _k_for_width(bi, layout, bn):
+    """A K that selects the built tile width `bn` (the width is a function of K)."""
+    for K in (256, 4096, 8192, 16384):
+        if bi.gemm_config(4096, K, torch.bfloat16, layout)[0] == bn:
+            return K
+    raise AssertionError("no K selects width %d" % bn)
 
 
 @pytest.mark.parametrize("dt", ["bf16", "fp16"])
-def test_tile_widths_all_selected(bi, dt):
-    w = _widths(bi)
-    assert {bn for (lay, bn) in w if lay == "linear"} == {64, 96, 128, 256}
-    assert {bn for (lay, bn) in w if lay == "matmul"} == {64, 128, 256}
+def test_tile_widths_depend_on_K_only(bi, dt):
+    for layout in ("linear", "matmul"):
+        widths = {bi.gemm_config(N, K, DT[dt], layout)[0]
+                  for N in (8, 4096, 11008, 14336, 38912) for K in (64, 4096)}
+        assert widths == {128}
+        assert bi.gemm_config(4096, 8192, DT[dt], layout)[0] == 256
 
 
 @pytest.mark.parametrize("dt", ["bf16", "fp16"])
-@pytest.mark.parametrize("layout_bn", ["linear-64", "linear-96", "linear-128", "linear-256",
-                                       "matmul-64", "matmul-128", "matmul-256"])
+@pytest.mark.parametrize("layout_bn", ["linear-128", "linear-256", "matmul-128", "matmul-256"])
 def test_16bit_parity_each_width(bi, dt, layout_bn):
     layout, bn = layout_bn.split("-")
-    N = _widths(bi)[(layout, int(bn))]
-    M, K = 300, 200          # three row tiles (ragged), four K blocks (ragged last block)
-    # sample 640 output columns: the first tile, one in the middle, the ragged end
+    K = _k_for_width(bi, layout, int(bn))
+    M, N = 300, 1000          # three row tiles (ragged), several column tiles (ragged)
     a, b, c = synth.gemm16(M, N, K, dt, seed=5, layout=layout, with_c=True)
     ad, bd, cd = _dev(a, b, c)
+    cols = np.r_[0:300, 600:1000]
     if layout == "linear":
         bias = synth.normal((N,), 6, 0.1, dt)
         y = bi.linear(ad, bd, bias.cuda())
-        cols = np.r_[0:256, N // 2 - 64:N // 2 + 64, N - 256:N]
         ref, nrm = oracle.linear(a, b[cols], bias[cols])
-        check_close(y[:, cols], ref, nrm, DT[dt], "linear bn=%s N=%d" % (bn, N))
+        check_close(y[:, cols], ref, nrm, DT[dt], "linear bn=%s K=%d" % (bn, K))
     else:
         y = bi.matmul(ad, bd)
-        cols = np.r_[0:256, N // 2 - 64:N // 2 + 64, N - 256:N]
         bs = b[:, cols].contiguous()
         ref, nrm = oracle.matmul(a, bs)
-        check_close(y[:, cols], ref, nrm, DT[dt], "matmul bn=%s N=%d" % (bn, N))
+        check_close(y[:, cols], ref, nrm, DT[dt], "matmul bn=%s K=%d" % (bn, K))
         ya = bi.addmm(cd, ad, bd, alpha=1.0, beta=1.0)
         ref, nrm = oracle.addmm(c[:, cols].contiguous(), a, bs, 1.0, 1.0)
         check_close(ya[:, cols], ref, nrm, DT[dt], "addmm bn=%s" % bn)
@@ -180,6 +178,19 @@ def test_c2_rows_invariant_across_batch(bi, dt, N):
     ref, nrm = oracle.addmm(c[rows][:, cols].cpu(), ah, bh, 1.0, 1.0)
     check_close(full_a[rows][:, cols], ref, nrm, DT[dt], "addmm N=%d sampled" % N)
     _no_device_error(bi)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "fp16"])
+def test_rows_invariant_wide_tile_k8192(bi, dt):
+    """The same row-bits property on the 256-column tile (K = 8192), M up to 512."""
+    a, b = synth.gemm16(512, 8192, 8192, dt, seed=12, device="cuda")
+    full = bi.matmul(a, b)
+    for M in C2_M:
+        assert_same_bits(bi.matmul(a[:M], b), full[:M], "matmul K=8192 M=%d" % M)
+    rows = [0, 300, 511]
+    cols = np.r_[0:64, 8128:8192]
+    ref, nrm = oracle.matmul(a[rows].cpu(), b[:, cols].contiguous().cpu())
+    check_close(full[rows][:, cols], ref, nrm, DT[dt], "K=8192 sampled")
 
 
 def test_c2_cublas_control_differs(bi):
