@@ -186,16 +186,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             // ------------------------------------------------ TMA producer
             prefetch_tmap(&tmA);
             prefetch_tmap(&tmB);
-            uint32_t it = 0;
+            // The A copy moves only the rows that exist (a_rows <= 128); tile rows past
+            // them are never stored, and no row's result depends on another row.
+            const uint32_t stage_tx = static_cast<uint32_t>(args.a_rows) * TC_BK * 2 + B_BYTES;
+            uint32_t it = 0, s = 0, ph = 0;
             bool ok = true;
             for (int64_t t = blockIdx.x; ok && t < total; t += gridDim.x) {
                 int64_t mb, nb;
                 tc_tile_coords(t, num_m, num_n, mb, nb);
                 for (int kb = 0; kb < KB; ++kb, ++it) {
-                    const uint32_t s = it % STAGES;
-                    const uint32_t ph = (it / STAGES) & 1u;
                     if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&full[s], A_BYTES + B_BYTES);
+                    mbar_arrive_expect_tx(&full[s], stage_tx);
                     tma_load_2d(sA + s * A_BYTES, &tmA, &full[s], kb * TC_BK,
                                 static_cast<int32_t>(mb * TC_BM));
                     if (!B_MN) {
@@ -219,6 +220,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                 tma_prefetch_2d(&tmB, static_cast<int32_t>(nb * BN + j * 64), kp);
                         }
                     }
+                    if (++s == STAGES) { s = 0; ph ^= 1u; }
                 }
             }
             if (!ok) {
@@ -231,7 +233,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------------ MMA issuer
-            uint32_t it = 0, tc = 0;
+            // Descriptors of stage 0; stage s adds s * (stage bytes >> 4) to the start
+            // address field, and K step j adds j * 32 bytes (K-major) or j * 2048
+            // bytes (MN-major B) the same way.
+            const uint64_t a_desc0 = smem_desc(smem_u32(sA), 16, 1024);
+            const uint64_t b_desc0 = B_MN ? smem_desc(smem_u32(sB), 8192, 1024)
+                                          : smem_desc(smem_u32(sB), 16, 1024);
+            constexpr uint64_t A_STEP = A_BYTES >> 4, B_STEP = B_BYTES >> 4;
+            constexpr uint64_t BK_STEP = B_MN ? (2048 >> 4) : (32 >> 4);
+            uint32_t tc = 0, s = 0, ph = 0;
             bool ok = true;
             for (int64_t t = blockIdx.x; ok && t < total; t += gridDim.x, ++tc) {
                 const uint32_t acc = tc & 1u;
@@ -239,21 +249,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int kb = 0; kb < KB; ++kb, ++it) {
-                    const uint32_t s = it % STAGES;
-                    const uint32_t ph = (it / STAGES) & 1u;
+                for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait(&full[s], ph, abort_flag)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_u32(sA + s * A_BYTES);
-                    const uint32_t b_addr = smem_u32(sB + s * B_BYTES);
+                    const uint64_t ad = a_desc0 + s * A_STEP;
+                    const uint64_t bd = b_desc0 + s * B_STEP;
 #pragma unroll
-                    for (int j = 0; j < TC_BK / 16; ++j) {
-                        const uint64_t ad = smem_desc(a_addr + j * 32, 16, 1024);
-                        const uint64_t bd = B_MN ? smem_desc(b_addr + j * 2048, 8192, 1024)
-                                                 : smem_desc(b_addr + j * 32, 16, 1024);
-                        mma_f16_ss(d_tmem, ad, bd, IDESC, (kb | j) != 0 ? 1u : 0u);
-                    }
+                    for (int j = 0; j < TC_BK / 16; ++j)
+                        mma_f16_ss(d_tmem, ad + j * (32 >> 4), bd + j * BK_STEP, IDESC,
+                                   (kb | j) != 0 ? 1u : 0u);
                     mma_commit(&empty[s]);
+                    if (++s == STAGES) { s = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
                 mma_commit(&tfull[acc]);
@@ -337,7 +343,7 @@ bi_status launch_gemm_tc_typed(const void *a, int64_t lda, const void *b, int64_
     {
         const uint64_t dims[2] = {static_cast<uint64_t>(args.K), static_cast<uint64_t>(args.M)};
         const uint64_t strides[1] = {static_cast<uint64_t>(lda) * 2};
-        const uint32_t box[2] = {TC_BK, TC_BM};
+        const uint32_t box[2] = {TC_BK, static_cast<uint32_t>(args.a_rows)};
         bi_status st = encode_tmap(&ta, dt, 2, const_cast<void *>(a), dims, strides, box, true);
         if (st != BI_OK) return st;
     }

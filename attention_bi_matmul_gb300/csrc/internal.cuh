@@ -23,6 +23,7 @@ struct GemmArgs {
     float alpha, beta; // EPI_ADDMM
     int epi;
     uint32_t *err;     // device error word
+    int a_rows;        // rows of A each copy moves: min(128, M rounded up to 16)
 };
 
 // Tile configuration of the tensor-core GEMM for one (N, K, dtype, layout).

@@ -3,6 +3,9 @@
   python -m attention_bi_matmul_gb300.profile_case linear M N K [--reps R]
   python -m attention_bi_matmul_gb300.profile_case matmul M N K [--reps R]
   python -m attention_bi_matmul_gb300.profile_case sdpa B H Hkv Lq Lkv [--reps R]
+  python -m attention_bi_matmul_gb300.profile_case sweep [--reps R]
+      (bf16 linear, K=4096, N in {4096, 11008, 14336}, M in {1,..,512}, each call
+      on one of 4 weight copies, as in the benchmark's batch sweep)
 
 Inputs are seeded synthetic bf16 tensors on cuda:0.  Prints the CUDA-event
 time per call of the last repetitions (not meaningful under a profiler).
@@ -23,8 +26,8 @@ if ROOT not in sys.path:
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("op", choices=("linear", "matmul", "sdpa"))
-    ap.add_argument("dims", type=int, nargs="+")
+    ap.add_argument("op", choices=("linear", "matmul", "sdpa", "sweep"))
+    ap.add_argument("dims", type=int, nargs="*")
     ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()
 
@@ -38,6 +41,20 @@ def main():
         y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         fn = (lambda: bi.linear(a, b, out=y)) if args.op == "linear" else (lambda: bi.matmul(a, b, out=y))
         work = "%.3f GFLOP" % (2.0 * M * N * K / 1e9)
+    elif args.op == "sweep":
+        Ns, Ms, K = (4096, 11008, 14336), (1, 2, 3, 4, 8, 16, 32, 64, 128, 256, 512), 4096
+        x = synth.normal((512, K), 0, 1.0 / math.sqrt(K), "bf16", dev)
+        ws = {N: [synth.normal((N, K), 10 * N + i, 1.0 / math.sqrt(K), "bf16", dev) for i in range(4)]
+              for N in Ns}
+        ys = {N: torch.empty((512, N), dtype=torch.bfloat16, device=dev) for N in Ns}
+
+        def fn():
+            i = 0
+            for N in Ns:
+                for M in Ms:
+                    bi.linear(x[:M], ws[N][i % 4], out=ys[N][:M])
+                    i += 1
+        work = "%.3f GB of weights" % (2.0 * len(Ms) * K * sum(Ns) / 1e9)
     else:
         B, H, Hkv, Lq, Lkv = args.dims
         q, k, v = synth.sdpa_qkv(B, H, Hkv, Lq, Lkv, 128, "bf16", seed=0, device=dev)
