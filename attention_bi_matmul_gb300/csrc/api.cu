@@ -157,7 +157,7 @@ TcConfig tc_config(int64_t N, int64_t K, bi_dtype dt, bool b_mn_major) {
     (void)b_mn_major;
     TcConfig c;
     c.block_n = K >= 8192 ? 256 : 128;
-    c.stages = c.block_n == 256 ? 4 : 6;
+    c.stages = c.block_n == 256 ? 4 : 3;    // ring depth (stages of 1 or 2 K panels)
     return c;
 }
 

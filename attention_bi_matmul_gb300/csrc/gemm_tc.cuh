@@ -18,9 +18,13 @@
 //     fp32 in a fixed order, one rounding to the output dtype.
 //
 // Roles (192 threads, persistent over output tiles):
-//   warp 0 lane 0  TMA producer
-//   warp 1         TMEM allocation; lane 0 issues the MMAs
+//   warp 0 lane 0  TMA producer (ring of STAGES stages; a stage holds KP
+//                  consecutive 64-wide K panels of A and of B)
+//   warp 1         TMEM allocation; lane 0 issues the MMAs (4 per panel)
 //   warps 2..5     epilogue (warp w reads TMEM lanes 32*(w%4) .. +31)
+// A stage of KP panels changes only how often the MMA thread waits and
+// commits, not the order of the MMAs: every output still sees its K = 16
+// steps in ascending order.
 // Two accumulator buffers in TMEM let the epilogue of tile i overlap the
 // mainloop of tile i+1.  The order in which tiles are visited never changes
 // any bit of the result.
@@ -102,7 +106,7 @@ __device__ __forceinline__ void gemm_epilogue32(const uint32_t (&r)[32], int64_t
 constexpr int TC_BM = 128;
 constexpr int TC_BK = 64;
 constexpr int TC_THREADS = 192;
-constexpr int TC_GROUP_M = 8;
+constexpr int TC_GROUP_M = 16;
 
 __host__ __device__ constexpr uint32_t tc_tmem_cols(int bn) {
     // two accumulator buffers of bn fp32 columns, rounded up to a power of two >= 32
@@ -110,9 +114,17 @@ __host__ __device__ constexpr uint32_t tc_tmem_cols(int bn) {
            : (2 * bn <= 256) ? 256u : 512u;
 }
 
-template <int BN, int STAGES>
+// Pipeline shape per tile width, 192 KB of shared memory in both cases:
+//   128 columns: stages of 2 K panels (8 MMAs of 64 cycles per barrier round trip), 3 stages;
+//   256 columns: stages of 1 K panel (4 MMAs of 128 cycles), 4 stages.
+template <int BN> __host__ __device__ constexpr int tc_kp() { return BN <= 128 ? 2 : 1; }
+template <int BN> __host__ __device__ constexpr int tc_stages() { return BN <= 128 ? 3 : 4; }
+template <int BN> __host__ __device__ constexpr bool tc_l2_prefetch() { return BN <= 128; }
+
+template <int BN>
 __host__ __device__ constexpr size_t tc_smem_bytes() {
-    return 1024 /* alignment slack */ + (size_t)STAGES * (TC_BM * TC_BK * 2 + BN * TC_BK * 2) +
+    return 1024 /* alignment slack */ +
+           (size_t)tc_stages<BN>() * tc_kp<BN>() * (TC_BM * TC_BK * 2 + BN * TC_BK * 2) +
            256 /* barriers etc */;
 }
 
@@ -128,12 +140,15 @@ __device__ __forceinline__ void tc_tile_coords(int64_t t, int64_t num_m, int64_t
     nb = r / gm;
 }
 
-template <typename T, int BN, int STAGES, bool B_MN>
+template <typename T, int BN, bool B_MN>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmArgs args) {
-    constexpr uint32_t A_BYTES = TC_BM * TC_BK * 2;
-    constexpr uint32_t B_BYTES = BN * TC_BK * 2;
+    constexpr int KP = tc_kp<BN>(), STAGES = tc_stages<BN>();
+    constexpr uint32_t A_PANEL = TC_BM * TC_BK * 2;   // 16 KB
+    constexpr uint32_t B_PANEL = BN * TC_BK * 2;
+    constexpr uint32_t A_BYTES = KP * A_PANEL;        // per stage
+    constexpr uint32_t B_BYTES = KP * B_PANEL;
     constexpr uint32_t TMEM_COLS = tc_tmem_cols(BN);
     constexpr uint32_t IDESC = mma_idesc(IsBf16<T>::value, TC_BM, BN, B_MN);
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile width");
@@ -159,7 +174,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int64_t num_m = (M + TC_BM - 1) / TC_BM;
     const int64_t num_n = (N + BN - 1) / BN;
     const int64_t total = num_m * num_n;
-    const int KB = static_cast<int>((K + TC_BK - 1) / TC_BK);
+    const int KB = static_cast<int>((K + KP * TC_BK - 1) / (KP * TC_BK));   // stages per tile
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -190,7 +205,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             prefetch_tmap(&tmB);
             // The A copy moves only the rows that exist (a_rows <= 128); tile rows past
             // them are never stored, and no row's result depends on another row.
-            const uint32_t stage_tx = static_cast<uint32_t>(args.a_rows) * TC_BK * 2 + B_BYTES;
+            const uint32_t tx = KP * (static_cast<uint32_t>(args.a_rows) * TC_BK * 2 + B_PANEL);
             uint32_t it = 0, s = 0, ph = 0;
             bool ok = true;
             for (int64_t t = blockIdx.x; ok && t < total; t += gridDim.x) {
@@ -198,28 +213,37 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 tc_tile_coords(t, num_m, num_n, mb, nb);
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&full[s], stage_tx);
-                    tma_load_2d(sA + s * A_BYTES, &tmA, &full[s], kb * TC_BK,
-                                static_cast<int32_t>(mb * TC_BM));
-                    if (!B_MN) {
-                        tma_load_2d(sB + s * B_BYTES, &tmB, &full[s], kb * TC_BK,
-                                    static_cast<int32_t>(nb * BN));
-                    } else {
+                    mbar_arrive_expect_tx(&full[s], tx);
 #pragma unroll
-                        for (int j = 0; j < BN / 64; ++j)
-                            tma_load_2d(sB + s * B_BYTES + j * 8192, &tmB, &full[s],
-                                        static_cast<int32_t>(nb * BN + j * 64), kb * TC_BK);
-                    }
-                    // Weight tiles a ring's depth further on start moving into L2 now, so that
-                    // a block streaming weights keeps twice the ring's bytes in flight.
-                    if (kb + STAGES < KB) {
-                        const int32_t kp = (kb + STAGES) * TC_BK;
+                    for (int p = 0; p < KP; ++p) {
+                        const int32_t k0 = (kb * KP + p) * TC_BK;   // beyond K: zero-filled
+                        tma_load_2d(sA + s * A_BYTES + p * A_PANEL, &tmA, &full[s], k0,
+                                    static_cast<int32_t>(mb * TC_BM));
                         if (!B_MN) {
-                            tma_prefetch_2d(&tmB, kp, static_cast<int32_t>(nb * BN));
+                            tma_load_2d(sB + s * B_BYTES + p * B_PANEL, &tmB, &full[s], k0,
+                                        static_cast<int32_t>(nb * BN));
                         } else {
 #pragma unroll
                             for (int j = 0; j < BN / 64; ++j)
-                                tma_prefetch_2d(&tmB, static_cast<int32_t>(nb * BN + j * 64), kp);
+                                tma_load_2d(sB + s * B_BYTES + p * B_PANEL + j * 8192, &tmB,
+                                            &full[s], static_cast<int32_t>(nb * BN + j * 64), k0);
+                        }
+                    }
+                    // 128-column tiles stream their weight panels from HBM with a short
+                    // ring; ask for the panels one ring further on to move into L2 now.
+                    // (Measured: +2-5% for those; it costs the L2-resident 256-wide
+                    // tiles 7%, so they do not.)
+                    if (tc_l2_prefetch<BN>() && kb + STAGES < KB) {
+#pragma unroll
+                        for (int p = 0; p < KP; ++p) {
+                            const int32_t kq = ((kb + STAGES) * KP + p) * TC_BK;
+                            if (!B_MN) {
+                                tma_prefetch_2d(&tmB, kq, static_cast<int32_t>(nb * BN));
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < BN / 64; ++j)
+                                    tma_prefetch_2d(&tmB, static_cast<int32_t>(nb * BN + j * 64), kq);
+                            }
                         }
                     }
                     if (++s == STAGES) { s = 0; ph ^= 1u; }
@@ -242,6 +266,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const uint64_t b_desc0 = B_MN ? smem_desc(smem_u32(sB), 8192, 1024)
                                           : smem_desc(smem_u32(sB), 16, 1024);
             constexpr uint64_t A_STEP = A_BYTES >> 4, B_STEP = B_BYTES >> 4;
+            constexpr uint64_t AP_STEP = A_PANEL >> 4, BP_STEP = B_PANEL >> 4;
             constexpr uint64_t BK_STEP = B_MN ? (2048 >> 4) : (32 >> 4);
             uint32_t tc = 0, s = 0, ph = 0;
             bool ok = true;
@@ -257,9 +282,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     const uint64_t ad = a_desc0 + s * A_STEP;
                     const uint64_t bd = b_desc0 + s * B_STEP;
 #pragma unroll
-                    for (int j = 0; j < TC_BK / 16; ++j)
-                        mma_f16_ss(d_tmem, ad + j * (32 >> 4), bd + j * BK_STEP, IDESC,
-                                   (kb | j) != 0 ? 1u : 0u);
+                    for (int p = 0; p < KP; ++p)
+#pragma unroll
+                        for (int j = 0; j < TC_BK / 16; ++j)
+                            mma_f16_ss(d_tmem, ad + p * AP_STEP + j * (32 >> 4),
+                                       bd + p * BP_STEP + j * BK_STEP, IDESC,
+                                       (kb | p | j) != 0 ? 1u : 0u);
                     mma_commit(&empty[s]);
                     if (++s == STAGES) { s = 0; ph ^= 1u; }
                 }
@@ -270,7 +298,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             mma_commit(mma_done);
             mbar_wait_limited(mma_done, 0, WAIT_LIMIT_NS);
         }
-    } else {
+    } else if (warp >= 2 && warp <= 5) {
         // ------------------------------------------------ epilogue (warps 2..5)
         const uint32_t quarter = static_cast<uint32_t>(warp & 3);
         const int row_in_tile = static_cast<int>(quarter) * 32 + lane;
@@ -308,15 +336,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 template <typename T, int BN, bool B_MN>
 bi_status launch_tc_inst(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &args,
                          int stages_req, cudaStream_t s) {
-    // Stage count is a function of BN only (chosen so the ring fills ~190 KB).
-    constexpr int STAGES = (BN <= 64) ? 8 : (BN <= 96) ? 7 : (BN <= 128) ? 6 : 4;
     (void)stages_req;
-    constexpr size_t SMEM = tc_smem_bytes<BN, STAGES>();
+    constexpr size_t SMEM = tc_smem_bytes<BN>();
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (!attr_set[dev & 63]) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<T, BN, STAGES, B_MN>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<T, BN, B_MN>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(SMEM));
         if (e != cudaSuccess) return cuda_status(e);
@@ -325,15 +351,11 @@ bi_status launch_tc_inst(const CUtensorMap &ta, const CUtensorMap &tb, const Gem
     const int64_t tiles = ((args.M + TC_BM - 1) / TC_BM) * ((args.N + BN - 1) / BN);
     const int sms = device_sm_count();
     const int grid = static_cast<int>(tiles < sms ? tiles : sms);
-    gemm_tc_kernel<T, BN, STAGES, B_MN><<<grid, TC_THREADS, SMEM, s>>>(ta, tb, args);
+    gemm_tc_kernel<T, BN, B_MN><<<grid, TC_THREADS, SMEM, s>>>(ta, tb, args);
     count_launch();
     return cuda_status(cudaGetLastError());
 }
 
-template <int BN>
-constexpr int tc_stages_for() {
-    return (BN <= 64) ? 8 : (BN <= 96) ? 7 : (BN <= 128) ? 6 : 4;
-}
 
 // Dispatch on the configured tile width; builds the tensor maps.
 template <typename T>

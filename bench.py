@@ -230,29 +230,27 @@ def capture(parts, bi):
     return graphs, bi.launch_count() - n0
 
 
-def batch_sweep_per_call(wl, bi, hbm, reps=20):
-    """Device time of each batch-sweep call alone (graph replay, rotating weight copies)."""
+def batch_sweep_per_call(wl, bi, hbm, reps=10, calls=8):
+    """Device time per call of each batch-sweep shape: a graph of `calls` back-to-back calls
+    cycling through the 4 weight copies, replayed `reps` times (as the step issues them)."""
     import torch
     out = []
     for N in C2_N:
         for M in C2_M:
-            gs = []
-            for i in range(WCOPIES):
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g):
-                    bi.linear(wl.x[:M], wl.w[N][i], out=wl.y[N][:M])
-                gs.append(g)
-            for g in gs:
-                g.replay()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for i in range(calls):
+                    bi.linear(wl.x[:M], wl.w[N][i % WCOPIES], out=wl.y[N][:M])
+            g.replay()
             torch.cuda.synchronize()
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record()
             for r in range(reps):
-                gs[r % WCOPIES].replay()
+                g.replay()
             e1.record()
             torch.cuda.synchronize()
-            us = e0.elapsed_time(e1) * 1e3 / reps
+            us = e0.elapsed_time(e1) * 1e3 / (reps * calls)
             gbs = 2.0 * (N * C2_K + M * C2_K + M * N) / (us * 1e-6) / 1e9
             out.append({"N": N, "M": M, "us": round(us, 2), "gbs": round(gbs, 1),
                         "frac_hbm": round(gbs / hbm, 3)})
@@ -401,7 +399,7 @@ def run_ours(args):
     st, code = bi.last_device_error()
     if st != 0:
         raise RuntimeError("device error word %#x after the timed region" % code)
-    per_call = None if args.eager else batch_sweep_per_call(wl, bi, hbm)
+    per_call = batch_sweep_per_call(wl, bi, hbm) if args.per_call else None
 
     flops = step_flops()
     byts = step_bytes()
@@ -581,6 +579,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip timing the CPU oracle (for profiling runs)")
+    ap.add_argument("--per-call", action="store_true",
+                    help="also report the device time of every batch-sweep shape")
     ap.add_argument("--eager", action="store_true",
                     help="time eager Python calls instead of CUDA-graph replays of each part")
     args = ap.parse_args()

@@ -45,7 +45,7 @@ def test_gemm_config_ignores_M_and_is_host_only(lib):
                 assert lib.bi_gemm_config(N, K, L.BI_BF16, layout, ctypes.byref(bn),
                                           ctypes.byref(st)) == L.BI_OK
                 assert bn.value == (256 if K >= 8192 else 128)
-                assert st.value == (4 if bn.value == 256 else 6)
+                assert st.value == (4 if bn.value == 256 else 3)
     assert lib.bi_gemm_config(0, 4096, L.BI_BF16, 0, None, None) == L.BI_ERR_INVALID_ARG
     assert lib.bi_gemm_config(64, 64, 7, 0, None, None) == L.BI_ERR_UNSUPPORTED
 
