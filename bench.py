@@ -499,7 +499,8 @@ def load_traffic(part: str):
     try:
         with open(path) as f:
             t = json.load(f)
-        return t.get(part)
+        v = t.get(part)
+        return float(v) if isinstance(v, (int, float)) else None
     except Exception:
         return None
 
