@@ -51,7 +51,13 @@ bool load_encode() {
     return true;
 }
 
-// The code in this library is built for sm_103a only.
+int g_ready[MAX_DEV] = {};     // per-device initialisation done
+
+bi_status device_init(int dev);
+
+// The code in this library is built for sm_103a only.  The first call on a
+// device also initialises everything later calls need on it (see device_init),
+// so that no later call makes a non-stream CUDA call.
 bi_status check_device() {
     const int dev = current_device();
     if (dev < 0) return BI_ERR_CUDA;
@@ -62,7 +68,13 @@ bi_status check_device() {
             return BI_ERR_CUDA;
         g_arch_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
     }
-    return g_arch_ok[dev] == 1 ? BI_OK : BI_ERR_UNSUPPORTED;
+    if (g_arch_ok[dev] != 1) return BI_ERR_UNSUPPORTED;
+    if (!g_ready[dev]) {
+        bi_status st = device_init(dev);
+        if (st != BI_OK) return st;
+        g_ready[dev] = 1;
+    }
+    return BI_OK;
 }
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -90,6 +102,28 @@ bi_status check_gemm(const void *a, int64_t lda, const void *b, int64_t ldb, voi
 
 bi_status run_gemm(const void *a, int64_t lda, const void *b, int64_t ldb, bool b_nk,
                    GemmArgs &args, bi_dtype dt, cudaStream_t s);
+
+}  // namespace
+
+uint32_t *device_error_word();
+int device_sm_count();
+
+namespace {
+
+// Everything a call may need on this device, done once: the shared-memory
+// attribute of every kernel, the device error word's address, the SM count and
+// the tensor-map encoder.
+bi_status device_init(int dev) {
+    (void)dev;
+    bi_status st;
+    if ((st = init_gemm_tc_bf16()) != BI_OK) return st;
+    if ((st = init_gemm_tc_f16()) != BI_OK) return st;
+    if ((st = init_sdpa()) != BI_OK) return st;
+    if (!device_error_word()) return BI_ERR_CUDA;
+    device_sm_count();
+    if (!load_encode()) return BI_ERR_CUDA;
+    return BI_OK;
+}
 
 }  // namespace
 

@@ -333,21 +333,28 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 }
 
 // Host side: instantiate and launch one configuration.
+// Shared-memory attribute of one instantiation (per device; done at library init).
+template <typename T, int BN, bool B_MN>
+bi_status init_tc_inst() {
+    return cuda_status(cudaFuncSetAttribute(gemm_tc_kernel<T, BN, B_MN>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            static_cast<int>(tc_smem_bytes<BN>())));
+}
+
+template <typename T>
+bi_status init_tc_all() {
+    bi_status st;
+    if ((st = init_tc_inst<T, 128, false>()) != BI_OK) return st;
+    if ((st = init_tc_inst<T, 256, false>()) != BI_OK) return st;
+    if ((st = init_tc_inst<T, 128, true>()) != BI_OK) return st;
+    return init_tc_inst<T, 256, true>();
+}
+
 template <typename T, int BN, bool B_MN>
 bi_status launch_tc_inst(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &args,
                          int stages_req, cudaStream_t s) {
     (void)stages_req;
     constexpr size_t SMEM = tc_smem_bytes<BN>();
-    static bool attr_set[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (!attr_set[dev & 63]) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<T, BN, B_MN>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(SMEM));
-        if (e != cudaSuccess) return cuda_status(e);
-        attr_set[dev & 63] = true;
-    }
     const int64_t tiles = ((args.M + TC_BM - 1) / TC_BM) * ((args.N + BN - 1) / BN);
     const int sms = device_sm_count();
     const int grid = static_cast<int>(tiles < sms ? tiles : sms);

@@ -8,4 +8,6 @@ bi_status launch_gemm_tc_f16(const void *a, int64_t lda, const void *b, int64_t 
     return launch_gemm_tc_typed<__half>(a, lda, b, ldb, b_nk, args, BI_F16, cfg, s);
 }
 
+bi_status init_gemm_tc_f16() { return init_tc_all<__half>(); }
+
 }  // namespace bi

@@ -42,6 +42,11 @@ bi_status encode_tmap(CUtensorMap *map, bi_dtype dt, int rank, void *base,
 TcConfig tc_config(int64_t N, int64_t K, bi_dtype dt, bool b_mn_major);
 bi_status cuda_status(cudaError_t e);
 
+// ---- per-device initialisation of each translation unit (kernel attributes)
+bi_status init_gemm_tc_bf16();
+bi_status init_gemm_tc_f16();
+bi_status init_sdpa();
+
 // ---- launchers
 bi_status launch_gemm_f32(const float *a, int64_t lda, const float *b, int64_t ldb, bool b_nk,
                           const GemmArgs &args, cudaStream_t s);

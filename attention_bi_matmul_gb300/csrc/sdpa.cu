@@ -433,16 +433,6 @@ __global__ void __launch_bounds__(SD_THREADS, 1)
 template <typename T>
 bi_status launch_sdpa_typed(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             const SdpaArgs &args, cudaStream_t s) {
-    static bool attr_set[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (!attr_set[dev & 63]) {
-        cudaError_t e = cudaFuncSetAttribute(sdpa_kernel<T>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(SD_SMEM_BYTES));
-        if (e != cudaSuccess) return cuda_status(e);
-        attr_set[dev & 63] = true;
-    }
     const int64_t t_first = args.q_offset / args.qt;
     const int64_t t_last = (args.q_offset + args.Lq - 1) / args.qt;
     const int64_t tiles = t_last - t_first + 1;
@@ -455,6 +445,16 @@ bi_status launch_sdpa_typed(const CUtensorMap &tq, const CUtensorMap &tk, const 
 }
 
 }  // namespace
+
+bi_status init_sdpa() {
+    bi_status st = cuda_status(cudaFuncSetAttribute(sdpa_kernel<__nv_bfloat16>,
+                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                    static_cast<int>(SD_SMEM_BYTES)));
+    if (st != BI_OK) return st;
+    return cuda_status(cudaFuncSetAttribute(sdpa_kernel<__half>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            static_cast<int>(SD_SMEM_BYTES)));
+}
 
 bi_status launch_sdpa(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                       const SdpaArgs &args, bi_dtype dt, cudaStream_t s) {

@@ -65,6 +65,37 @@ def load_peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+# ------------------------------------------------------------------ ranks
+
+def rank_info():
+    """(rank, local rank, world size) from the torchrun environment (1 process if unset)."""
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """The maximum of x over all ranks (x itself without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(step_flops: float, ms_per_step: float, world: int) -> float:
+    """TFLOP/s of all replicas together: every rank runs the same step on its own GPU
+    (the path has no cross-GPU exchange), timed by the slowest rank."""
+    return world * step_flops / (ms_per_step * 1e-3) / 1e12
+
+
+def emit(out: dict, rank: int):
+    """Only rank 0 prints the result line."""
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
 # ------------------------------------------------------------------ work accounting
 
 def step_flops():
@@ -317,9 +348,7 @@ def run_ours(args):
     import torch
     import torch.distributed as dist
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    rank, local, world = rank_info()
     if world > 1:
         dist.init_process_group("nccl", init_method="env://")
     torch.cuda.set_device(local)
@@ -391,10 +420,7 @@ def run_ours(args):
     ms_total = start.elapsed_time(stop)
     part_ms = [sum(ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(K)) / K
                for i in range(len(parts))]
-    t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_per_step = float(t.item()) / K
+    ms_per_step = max_over_ranks(ms_total, dev) / K
 
     st, code = bi.last_device_error()
     if st != 0:
@@ -404,7 +430,7 @@ def run_ours(args):
     flops = step_flops()
     byts = step_bytes()
     step_f = sum(flops.values())
-    value = world * step_f / (ms_per_step * 1e-3) / 1e12
+    value = whole_job_value(step_f, ms_per_step, world)
 
     pinfo = {}
     for name, ms in zip(Workload.PARTS, part_ms):
@@ -457,10 +483,7 @@ def run_ours(args):
         e2e_step(bi, host, dev)
     e1.record()
     torch.cuda.synchronize()
-    te = torch.tensor([e0.elapsed_time(e1) / Ke], device=dev, dtype=torch.float64)
-    if world > 1:
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-    e2e_val = world * step_f / (float(te.item()) * 1e-3) / 1e12
+    e2e_val = whole_job_value(step_f, max_over_ranks(e0.elapsed_time(e1) / Ke, dev), world)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -487,7 +510,7 @@ def run_ours(args):
                        "d2h_bytes_per_step": d2h},
                "gpu_launches": launches, "clocks": clocks,
                "batch_sweep_per_call": per_call}
-        print(json.dumps(out), flush=True)
+        emit(out, rank)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
@@ -508,10 +531,9 @@ def load_traffic(part: str):
 # ------------------------------------------------------------------ reference arm (the oracle)
 
 def run_reference(args):
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
+    rank, _, world = rank_info()
     if rank != 0:
-        return
+        return          # under torchrun only rank 0 times the oracle; the others exit 0
     import torch
     import oracle
     from attention_bi_matmul_gb300 import synth
@@ -532,7 +554,8 @@ def run_reference(args):
     xd = oracle._f64(x)
     qd, kd, vd = oracle._f64(q), oracle._f64(k), oracle._f64(v)
     total = args.steps + args.warmup
-    budget = max(0.3, 150.0 / max(total, 1))   # the whole run stays within a few minutes
+    # per-step CPU budget: the whole run stays within a few minutes
+    budget = args.budget_s if args.budget_s else max(0.3, 150.0 / max(total, 1))
     # calibrate rows of the big GEMM per step
     t = time.perf_counter()
     oracle.linear(oracle._f64(X[:8]), Wd)
@@ -569,7 +592,7 @@ def run_reference(args):
            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": oracle.num_threads(),
                             "kind": "oracle", "sample": sample},
            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    print(json.dumps(out), flush=True)
+    emit(out, rank)
 
 
 def main():
@@ -580,6 +603,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip timing the CPU oracle (for profiling runs)")
+    ap.add_argument("--budget-s", type=float, default=0.0,
+                    help="reference arm: CPU seconds per step (default: fit the run in ~2.5 min)")
     ap.add_argument("--per-call", action="store_true",
                     help="also report the device time of every batch-sweep shape")
     ap.add_argument("--eager", action="store_true",

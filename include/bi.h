@@ -26,6 +26,11 @@
  *
  * Errors reported by the device (a bounded wait that ran out) are recorded in
  * a library-owned device error word and read with bi_last_device_error().
+ *
+ * First use: the first call that reaches a kernel on a device initialises the
+ * library's per-device state (kernel shared-memory attributes, the error word's
+ * address, the tensor-map encoder).  Make that first call before capturing a
+ * CUDA graph on the device; every later call makes only stream launches.
  */
 #ifndef BI_H
 #define BI_H
