@@ -71,6 +71,9 @@ class Oracle:
                                      ctypes.c_double, ctypes.c_double, _D, _D]
         lib.oracle_sdpa.argtypes = [_I64, _I64, _I64, _I64, _I64, _I64, _D, _D, _D,
                                     ctypes.c_double, ctypes.c_int, _I64, _D, _D]
+        lib.oracle_sdpa_ex.argtypes = [_I64, _I64, _I64, _I64, _I64, _I64, _D, _D, _D,
+                                       ctypes.c_double, ctypes.c_int, _I64, _D,
+                                       ctypes.POINTER(ctypes.c_ubyte), _D, _D]
         lib.oracle_rmsnorm.argtypes = [_I64, _I64, _D, _D, ctypes.c_double, _D]
         lib.oracle_rope.argtypes = [_I64, _I64, _I64, _D, ctypes.POINTER(ctypes.c_int64),
                                     ctypes.c_double, _D]
@@ -133,6 +136,32 @@ class Oracle:
                              1 if causal else 0, int(q_offset), _p(o), _p(nrm))
         return o, nrm
 
+    def sdpa_ex(self, q, k, v, causal=True, q_offset=None, scale=None, sinks=None, mask=None):
+        """sdpa with optional attention sinks (sinks[H], logits in the units of the scaled
+        scores) and an optional boolean array mask [B,H,Lq,Lkv] (or broadcastable to it),
+        nonzero = visible; a mask overrides `causal`."""
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        B, H, Lq, D = q.shape
+        Hkv, Lkv = k.shape[1], k.shape[2]
+        assert k.shape == (B, Hkv, Lkv, D) and v.shape == k.shape and H % Hkv == 0
+        if q_offset is None:
+            q_offset = Lkv - Lq
+        if scale is None:
+            scale = 1.0 / np.sqrt(D)
+        sk = None if sinks is None else _f64(sinks).reshape(H)
+        mk = None
+        if mask is not None:
+            if hasattr(mask, "detach"):
+                mask = mask.detach().to("cpu").numpy()
+            mk = np.ascontiguousarray(np.broadcast_to(np.asarray(mask) != 0, (B, H, Lq, Lkv)),
+                                      dtype=np.uint8)
+        o = np.empty((B, H, Lq, D)); nrm = np.empty((B, H, Lq, D))
+        self.lib.oracle_sdpa_ex(B, H, Hkv, Lq, Lkv, D, _p(q), _p(k), _p(v), float(scale),
+                                1 if causal else 0, int(q_offset), _p(sk),
+                                None if mk is None else mk.ctypes.data_as(ctypes.POINTER(ctypes.c_ubyte)),
+                                _p(o), _p(nrm))
+        return o, nrm
+
     def rmsnorm(self, x, w, eps=1e-6):
         """y = x / sqrt(mean(x^2) + eps) * w over the last dim; x[M,N], w[N]."""
         x, w = _f64(x), _f64(w)
@@ -191,6 +220,10 @@ def addmm(c, a, b, alpha=1.0, beta=1.0):
 
 def sdpa(q, k, v, causal=True, q_offset=None, scale=None):
     return default().sdpa(q, k, v, causal, q_offset, scale)
+
+
+def sdpa_ex(q, k, v, causal=True, q_offset=None, scale=None, sinks=None, mask=None):
+    return default().sdpa_ex(q, k, v, causal, q_offset, scale, sinks, mask)
 
 
 def rmsnorm(x, w, eps=1e-6):

@@ -18,14 +18,19 @@
  *   - "Accuracy": the results are judged against a float64 reference; this is
  *     that reference.
  *   - "Why MLX is not invariant" / Attention: GQA (H query heads share Hkv
- *     key/value heads).
+ *     key/value heads); "How the kernels work" / Attention: "all three mask
+ *     forms" (none, causal, array); the last paragraph before "Prior art":
+ *     attention sinks.
  * Readings where the page is silent (each also listed in the design notes):
  *   - causal alignment: query i sits at absolute position q_offset + i and sees
  *     key j iff j <= q_offset + i;
  *   - GQA head map: query head h reads key/value head h / (H / Hkv);
  *   - addmm: y = beta * c + alpha * (a . b), c either [M,N] or a row c[N];
  *   - RoPE: rotate-half pairing, inv_freq_i = base^(-2i/D);
- *   - SwiGLU: input [M, 2I] = [gate | up], y = silu(gate) * up.
+ *   - SwiGLU: input [M, 2I] = [gate | up], y = silu(gate) * up;
+ *   - array mask: boolean, nonzero = the key is visible;
+ *   - attention sink: one extra logit per query head, in the units of the
+ *     scaled scores, that joins the softmax denominator with no value.
  * Every function also returns the per-element normaliser that the tolerance
  * is stated against (the sum of the magnitudes of the terms).
  *
@@ -115,22 +120,29 @@ void oracle_addmm(int64_t M, int64_t N, int64_t K, const double *c, int c_row,
     }
 }
 
-/* Scaled dot-product attention with GQA, optionally causal.
+/* Scaled dot-product attention with GQA.
  *   q[B,H,Lq,D], k[B,Hkv,Lkv,D], v[B,Hkv,Lkv,D], o[B,H,Lq,D]; dense row-major.
  *   kv head of query head h: h / (H / Hkv).
- *   visible keys of query i: j < Lkv, and (causal) j <= q_offset + i.
- *   s_j = scale * <q_i, k_j>;  p = softmax(s) over the visible keys, computed
- *   as exp(s_j - max s) / sum exp(s - max s);  o_i = sum_j p_j v_j.
- *   nrm[b,h,i,d] = sum_j p_j |v_j[d]|.
- * A query with no visible key is a caller error; its output is set to NaN.  */
-void oracle_sdpa(int64_t B, int64_t H, int64_t Hkv, int64_t Lq, int64_t Lkv, int64_t D,
-                 const double *q, const double *k, const double *v, double scale,
-                 int causal, int64_t q_offset, double *o, double *nrm)
+ *   visible keys of query i: j < Lkv and
+ *     mask != NULL: mask[((b*H + h)*Lq + i)*Lkv + j] != 0   (boolean array mask)
+ *     else causal:  j <= q_offset + i
+ *     else:         every j.
+ *   s_j = scale * <q_i, k_j>.  With sinks != NULL, head h has one more logit
+ *   sinks[h] (in the units of s) that enters the softmax denominator and
+ *   carries no value.  p_j = exp(s_j - mx) / (sum_visible exp(s - mx)
+ *   [+ exp(sink_h - mx)]), mx the maximum of the visible s (and the sink);
+ *   o_i = sum_j p_j v_j;  nrm[b,h,i,d] = sum_j p_j |v_j[d]|.
+ * A query with no visible key and no sink has no defined output: NaN.      */
+void oracle_sdpa_ex(int64_t B, int64_t H, int64_t Hkv, int64_t Lq, int64_t Lkv, int64_t D,
+                    const double *q, const double *k, const double *v, double scale, int causal,
+                    int64_t q_offset, const double *sinks, const unsigned char *mask, double *o,
+                    double *nrm)
 {
     const int64_t group = H / Hkv;
 #pragma omp parallel
     {
         double *s = (double *)malloc(sizeof(double) * (size_t)(Lkv > 0 ? Lkv : 1));
+        unsigned char *vis = (unsigned char *)malloc((size_t)(Lkv > 0 ? Lkv : 1));
 #pragma omp for schedule(dynamic, 1) collapse(3)
         for (int64_t b = 0; b < B; ++b) {
             for (int64_t h = 0; h < H; ++h) {
@@ -141,33 +153,40 @@ void oracle_sdpa(int64_t B, int64_t H, int64_t Hkv, int64_t Lq, int64_t Lkv, int
                     const double *vb = v + (b * Hkv + hk) * Lkv * D;
                     double *oi = o + ((b * H + h) * Lq + i) * D;
                     double *ni = nrm ? nrm + ((b * H + h) * Lq + i) * D : 0;
-                    int64_t nvis = Lkv;
-                    if (causal) {
-                        int64_t last = q_offset + i; /* last visible key */
-                        nvis = last + 1 < Lkv ? last + 1 : Lkv;
+                    int64_t nvis = 0;
+                    for (int64_t j = 0; j < Lkv; ++j) {
+                        int visible;
+                        if (mask) visible = mask[((b * H + h) * Lq + i) * Lkv + j] != 0;
+                        else if (causal) visible = j <= q_offset + i;
+                        else visible = 1;
+                        vis[j] = (unsigned char)visible;
+                        nvis += visible;
                     }
-                    if (nvis <= 0) {
+                    if (nvis == 0 && !sinks) {
                         for (int64_t d = 0; d < D; ++d) {
                             oi[d] = NAN;
                             if (ni) ni[d] = NAN;
                         }
                         continue;
                     }
-                    double mx = -INFINITY;
-                    for (int64_t j = 0; j < nvis; ++j) {
+                    double mx = sinks ? sinks[h] : -INFINITY;
+                    for (int64_t j = 0; j < Lkv; ++j) {
+                        if (!vis[j]) continue;
                         double t = 0.0;
                         for (int64_t d = 0; d < D; ++d) t += qi[d] * kb[j * D + d];
                         s[j] = scale * t;
                         if (s[j] > mx) mx = s[j];
                     }
-                    double den = 0.0;
-                    for (int64_t j = 0; j < nvis; ++j) {
+                    double den = sinks ? exp(sinks[h] - mx) : 0.0;
+                    for (int64_t j = 0; j < Lkv; ++j) {
+                        if (!vis[j]) continue;
                         s[j] = exp(s[j] - mx);
                         den += s[j];
                     }
                     for (int64_t d = 0; d < D; ++d) {
                         double acc = 0.0, r = 0.0;
-                        for (int64_t j = 0; j < nvis; ++j) {
+                        for (int64_t j = 0; j < Lkv; ++j) {
+                            if (!vis[j]) continue;
                             double p = s[j] / den;
                             acc += p * vb[j * D + d];
                             r += p * fabs(vb[j * D + d]);
@@ -178,8 +197,17 @@ void oracle_sdpa(int64_t B, int64_t H, int64_t Hkv, int64_t Lq, int64_t Lkv, int
                 }
             }
         }
+        free(vis);
         free(s);
     }
+}
+
+/* The plain causal / unmasked form without sinks (the README's "Use" call). */
+void oracle_sdpa(int64_t B, int64_t H, int64_t Hkv, int64_t Lq, int64_t Lkv, int64_t D,
+                 const double *q, const double *k, const double *v, double scale,
+                 int causal, int64_t q_offset, double *o, double *nrm)
+{
+    oracle_sdpa_ex(B, H, Hkv, Lq, Lkv, D, q, k, v, scale, causal, q_offset, 0, 0, o, nrm);
 }
 
 /* RMSNorm over the last dim: y[m,n] = x[m,n] / sqrt(mean_n x[m,.]^2 + eps) * w[n] */

@@ -155,8 +155,9 @@ def pin_gemm_identities(O):
 
 # ------------------------------------------------------------------ attention pins
 
-def _decimal_sdpa(q, k, v, causal, q_offset, scale):
-    """Softmax attention in 60-digit decimal arithmetic, straight from the definition."""
+def _decimal_sdpa(q, k, v, causal, q_offset, scale, sinks=None, mask=None):
+    """Softmax attention in 60-digit decimal arithmetic, straight from the definition
+    (optional sink logit per head in the denominator, optional boolean mask)."""
     getcontext().prec = 60
     B, H, Lq, D = q.shape
     Hkv, Lkv = k.shape[1], k.shape[2]
@@ -168,13 +169,17 @@ def _decimal_sdpa(q, k, v, causal, q_offset, scale):
         for h in range(H):
             hk = h // G
             for i in range(Lq):
-                last = q_offset + i if causal else Lkv - 1
-                vis = [j for j in range(Lkv) if j <= last]
+                if mask is not None:
+                    vis = [j for j in range(Lkv) if mask[b, h, i, j]]
+                else:
+                    last = q_offset + i if causal else Lkv - 1
+                    vis = [j for j in range(Lkv) if j <= last]
                 s = [sc * sum(Decimal(q[b, h, i, d]) * Decimal(k[b, hk, j, d]) for d in range(D))
                      for j in vis]
-                mx = max(s)
+                sk = Decimal(sinks[h]) if sinks is not None else None
+                mx = max(s + ([sk] if sk is not None else []))
                 e = [(x - mx).exp() for x in s]
-                den = sum(e)
+                den = sum(e) + ((sk - mx).exp() if sk is not None else Decimal(0))
                 for d in range(D):
                     out[b, h, i, d] = float(sum(e[t] * Decimal(v[b, hk, j, d])
                                                 for t, j in enumerate(vis)) / den)
@@ -264,6 +269,74 @@ def pin_sdpa_structure(O):
     _close(a, b, 8 * Lkv * U64 * nrm + 1e-300, "key permutation without mask")
 
 
+def pin_sdpa_sinks_and_masks_bruteforce(O):
+    rng = _rng(14)
+    B, H, Hkv, Lq, Lkv, D = 2, 4, 2, 3, 6, 3
+    q = rng.standard_normal((B, H, Lq, D)); k = rng.standard_normal((B, Hkv, Lkv, D))
+    v = rng.standard_normal((B, Hkv, Lkv, D))
+    sinks = rng.standard_normal(H) * 2
+    mask = rng.random((B, H, Lq, Lkv)) < 0.6
+    mask[..., 0] |= ~mask.any(-1)            # every row sees at least one key
+    sc = 1.0 / math.sqrt(D)
+    for sk, mk, causal in ((sinks, None, True), (None, mask, True), (sinks, mask, False)):
+        o, nrm = O.sdpa_ex(q, k, v, causal=causal, q_offset=3, sinks=sk, mask=mk)
+        want, wmag = _decimal_sdpa(q, k, v, causal, 3, sc, sinks=sk, mask=mk)
+        _close(o, want, 1e-13 * wmag + 1e-300, "sdpa sinks/mask brute force")
+        _close(nrm, wmag, 1e-13 * wmag + 1e-300, "sdpa sinks/mask normaliser")
+
+
+def pin_sdpa_sinks_and_masks_torch(O):
+    """torch CPU float64 SDPA: a boolean mask directly; a sink as one extra key whose score
+    is 0 plus an additive mask value of sink_h, carrying a zero value vector."""
+    rng = _rng(15)
+    B, H, Hkv, Lq, Lkv, D = 2, 6, 3, 5, 19, 8
+    q = rng.standard_normal((B, H, Lq, D)); k = rng.standard_normal((B, Hkv, Lkv, D))
+    v = rng.standard_normal((B, Hkv, Lkv, D))
+    sinks = rng.standard_normal(H) * 1.5
+    mask = rng.random((B, H, Lq, Lkv)) < 0.5
+    mask[..., 3] = True
+    tq, tk, tv = (torch.from_numpy(t) for t in (q, k, v))
+    G = H // Hkv
+    tk, tv = tk.repeat_interleave(G, 1), tv.repeat_interleave(G, 1)
+    o, nrm = O.sdpa_ex(q, k, v, mask=mask)
+    want = F.scaled_dot_product_attention(tq, tk, tv, attn_mask=torch.from_numpy(mask)).numpy()
+    _close(o, want, 1e-12 * nrm + 1e-300, "array mask vs torch")
+    zk = torch.cat([tk, torch.zeros(B, H, 1, D, dtype=torch.float64)], 2)
+    zv = torch.cat([tv, torch.zeros(B, H, 1, D, dtype=torch.float64)], 2)
+    add = torch.zeros(B, H, Lq, Lkv + 1, dtype=torch.float64)
+    add[..., :Lkv] = torch.where(torch.from_numpy(mask), 0.0, float("-inf"))
+    add[..., Lkv] = torch.from_numpy(sinks)[None, :, None]
+    o, nrm = O.sdpa_ex(q, k, v, sinks=sinks, mask=mask)
+    want = F.scaled_dot_product_attention(tq, zk, zv, attn_mask=add).numpy()
+    _close(o, want, 1e-12 * np.maximum(nrm, 1e-3), "sinks vs torch extra-key form")
+
+
+def pin_sdpa_mask_structure(O):
+    """causal == the causal pattern as an array mask; an all-true mask == no mask; a sink of
+    -inf == no sink; one visible key with a sink: o = v_j * e^s / (e^s + e^sink)."""
+    rng = _rng(16)
+    B, H, Hkv, Lq, Lkv, D = 1, 4, 2, 4, 9, 8
+    q = rng.standard_normal((B, H, Lq, D)); k = rng.standard_normal((B, Hkv, Lkv, D))
+    v = rng.standard_normal((B, Hkv, Lkv, D))
+    causal_pat = (np.arange(Lkv)[None, :] <= 5 + np.arange(Lq)[:, None])[None, None]
+    a, _ = O.sdpa(q, k, v, causal=True, q_offset=5)
+    b, _ = O.sdpa_ex(q, k, v, mask=np.broadcast_to(causal_pat, (B, H, Lq, Lkv)))
+    assert np.array_equal(a, b), "causal == causal-pattern array mask"
+    a, _ = O.sdpa(q, k, v, causal=False)
+    b, _ = O.sdpa_ex(q, k, v, mask=np.ones((B, H, Lq, Lkv), bool))
+    assert np.array_equal(a, b), "all-true mask == no mask"
+    b, _ = O.sdpa_ex(q, k, v, causal=False, sinks=np.full(H, -np.inf))
+    assert np.array_equal(a, b), "sink -inf == no sink"
+    one = np.zeros((B, H, Lq, Lkv), bool); one[..., 2] = True
+    sk = rng.standard_normal(H)
+    o, _ = O.sdpa_ex(q, k, v, sinks=sk, mask=one)
+    for h in range(H):
+        for i in range(Lq):
+            s = (q[0, h, i] @ k[0, h // 2, 2]) / math.sqrt(D)
+            w = math.exp(s) / (math.exp(s) + math.exp(sk[h]))
+            _close(o[0, h, i], w * v[0, h // 2, 2], 1e-14 * np.abs(v).max(), "one key + sink")
+
+
 # ------------------------------------------------------------------ glue pins
 
 def pin_rmsnorm(O):
@@ -310,4 +383,6 @@ def pin_swiglu(O):
 ALL_PINS = [pin_linear_bruteforce, pin_matmul_bruteforce, pin_addmm_bruteforce,
             pin_gemm_integer_exact, pin_gemm_numpy, pin_gemm_identities,
             pin_sdpa_bruteforce, pin_sdpa_torch, pin_sdpa_closed_forms, pin_sdpa_structure,
+            pin_sdpa_sinks_and_masks_bruteforce, pin_sdpa_sinks_and_masks_torch,
+            pin_sdpa_mask_structure,
             pin_rmsnorm, pin_rope, pin_swiglu]

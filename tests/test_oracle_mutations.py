@@ -19,8 +19,14 @@ MUTATIONS = {
     "addmm_sign": ("beta * cv + alpha * s", "beta * cv - alpha * s"),
     "addmm_alpha_beta_swapped": ("beta * cv + alpha * s", "alpha * cv + beta * s"),
     "sdpa_gqa_map": ("const int64_t hk = h / group;", "const int64_t hk = h % Hkv;"),
-    "sdpa_causal_off_by_one": ("nvis = last + 1 < Lkv ? last + 1 : Lkv;",
-                               "nvis = last + 2 < Lkv ? last + 2 : Lkv;"),
+    "sdpa_causal_off_by_one": ("else if (causal) visible = j <= q_offset + i;",
+                               "else if (causal) visible = j <= q_offset + i + 1;"),
+    "sdpa_sink_not_in_denominator": ("double den = sinks ? exp(sinks[h] - mx) : 0.0;",
+                                     "double den = 0.0;"),
+    "sdpa_mask_ignored": ("if (mask) visible = mask[((b * H + h) * Lq + i) * Lkv + j] != 0;",
+                          "if (mask) visible = 1;"),
+    "sdpa_mask_transposed_heads": ("if (mask) visible = mask[((b * H + h) * Lq + i) * Lkv + j] != 0;",
+                                   "if (mask) visible = mask[((b * H + (H - 1 - h)) * Lq + i) * Lkv + j] != 0;"),
     "sdpa_exp_sign": ("s[j] = exp(s[j] - mx);", "s[j] = exp(mx - s[j]);"),
     "sdpa_no_scale": ("s[j] = scale * t;", "s[j] = t;"),
     "sdpa_normaliser": ("r += p * fabs(vb[j * D + d]);", "r += fabs(vb[j * D + d]);"),
