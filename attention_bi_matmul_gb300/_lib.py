@@ -30,6 +30,8 @@ SIGNATURES = {
                              ctypes.POINTER(_int)]),
     "bi_sdpa": (_st, [_vp, _i64p, _vp, _i64p, _vp, _i64p, _vp, _i64p, _i64, _i64, _i64, _i64,
                       _i64, _i64, _f, _int, _i64, _int, _vp]),
+    "bi_sdpa_ex": (_st, [_vp, _i64p, _vp, _i64p, _vp, _i64p, _vp, _i64p, _i64, _i64, _i64, _i64,
+                         _i64, _i64, _f, _int, _i64, _vp, _vp, _i64p, _int, _vp]),
     "bi_rmsnorm": (_st, [_vp, _i64, _vp, _vp, _i64, _i64, _i64, _f, _int, _vp]),
     "bi_rope": (_st, [_vp, _i64p, _vp, _i64p, _i64, _i64, _i64, _i64, _i64, _f, _int, _vp]),
     "bi_swiglu": (_st, [_vp, _i64, _vp, _i64, _i64, _i64, _int, _vp]),
@@ -45,7 +47,7 @@ SIGNATURES = {
 
 BI_OK, BI_ERR_INVALID_ARG, BI_ERR_UNSUPPORTED, BI_ERR_ALIGNMENT, BI_ERR_CUDA, BI_ERR_TIMEOUT = range(6)
 BI_F32, BI_F16, BI_BF16 = 0, 1, 2
-BI_MASK_NONE, BI_MASK_CAUSAL = 0, 1
+BI_MASK_NONE, BI_MASK_CAUSAL, BI_MASK_ARRAY = 0, 1, 2
 
 _lib = None
 

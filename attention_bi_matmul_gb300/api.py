@@ -173,12 +173,17 @@ def gemm_config(N: int, K: int, dtype=torch.bfloat16, layout: str = "linear"):
 
 def sdpa(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = True,
          q_offset: int | None = None, scale: float | None = None,
-         out: torch.Tensor | None = None) -> torch.Tensor:
+         out: torch.Tensor | None = None, mask: torch.Tensor | None = None,
+         sinks: torch.Tensor | None = None) -> torch.Tensor:
     """Attention, q[B,H,Lq,D], k/v[B,Hkv,Lkv,D] (any strides, last dim contiguous).
 
     Query i sits at absolute position q_offset + i (default Lkv - Lq); with
-    ``causal`` it sees keys j <= q_offset + i.  Returns o[B,H,Lq,D].
+    ``causal`` it sees keys j <= q_offset + i.  ``mask``: a boolean array mask
+    broadcastable to [B,H,Lq,Lkv] (True = visible; overrides ``causal``).
+    ``sinks``: fp32 [H] sink logits.  Returns o[B,H,Lq,D].
     """
+    if mask is not None or sinks is not None:
+        return _sdpa_ex(q, k, v, causal, q_offset, scale, out, mask, sinks)
     dev = _cuda(q, k, v, out)
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
         raise ValueError("sdpa: q, k, v must be 4-D")
@@ -196,6 +201,37 @@ def sdpa(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = True,
                                  B, H, Hkv, Lq, Lkv, D, 0.0 if scale is None else float(scale),
                                  L.BI_MASK_CAUSAL if causal else L.BI_MASK_NONE, qo, _dt(q), s),
                 "bi_sdpa")
+    return o
+
+
+def _sdpa_ex(q, k, v, causal, q_offset, scale, out, mask, sinks):
+    dev = _cuda(q, k, v, out, mask, sinks)
+    B, H, Lq, D = q.shape
+    Hkv, Lkv = k.shape[1], k.shape[2]
+    if k.shape != (B, Hkv, Lkv, D) or v.shape != k.shape:
+        raise ValueError("sdpa: k/v must be [B, Hkv, Lkv, D]")
+    mode = L.BI_MASK_CAUSAL if causal else L.BI_MASK_NONE
+    mptr, ms = None, None
+    if mask is not None:
+        if mask.dtype != torch.bool:
+            raise ValueError("sdpa: the array mask must be boolean (True = visible)")
+        m4 = mask.reshape((1,) * (4 - mask.dim()) + tuple(mask.shape)) if mask.dim() < 4 else mask
+        m4 = m4.expand(B, H, Lq, Lkv)
+        if m4.stride(-1) != 1:
+            raise ValueError("sdpa: the mask's last dimension must be contiguous")
+        mode, mptr, ms = L.BI_MASK_ARRAY, ctypes.c_void_p(m4.data_ptr()), L.i64arr(m4.stride())
+    sk = None
+    if sinks is not None:
+        if sinks.dtype != torch.float32 or sinks.shape != (H,) or not sinks.is_contiguous():
+            raise ValueError("sdpa: sinks must be contiguous float32 [H]")
+        sk = ctypes.c_void_p(sinks.data_ptr())
+    o = torch.empty((B, H, Lq, D), dtype=q.dtype, device=q.device) if out is None else out
+    qo = -1 if q_offset is None else int(q_offset)
+    with _On(dev) as s:
+        L.check(L.load().bi_sdpa_ex(_p(q), L.i64arr(q.stride()), _p(k), L.i64arr(k.stride()),
+                                    _p(v), L.i64arr(v.stride()), _p(o), L.i64arr(o.stride()),
+                                    B, H, Hkv, Lq, Lkv, D, 0.0 if scale is None else float(scale),
+                                    mode, qo, sk, mptr, ms, _dt(q), s), "bi_sdpa_ex")
     return o
 
 

@@ -287,16 +287,24 @@ bi_status bi_gemm_config(int64_t N, int64_t K, bi_dtype dtype, int b_layout, int
     return BI_OK;
 }
 
-bi_status bi_sdpa(const void *q, const int64_t qs[4], const void *k, const int64_t ks[4],
-                  const void *v, const int64_t vs[4], void *o, const int64_t os[4], int64_t B,
-                  int64_t H, int64_t Hkv, int64_t Lq, int64_t Lkv, int64_t D, float scale,
-                  bi_mask mask, int64_t q_offset, bi_dtype dtype, bi_stream_t stream) {
-    if (dtype != BI_BF16 && dtype != BI_F16) return valid_dtype(dtype) ? BI_ERR_UNSUPPORTED
-                                                                         : BI_ERR_UNSUPPORTED;
+bi_status bi_sdpa_ex(const void *q, const int64_t qs[4], const void *k, const int64_t ks[4],
+                     const void *v, const int64_t vs[4], void *o, const int64_t os[4], int64_t B,
+                     int64_t H, int64_t Hkv, int64_t Lq, int64_t Lkv, int64_t D, float scale,
+                     bi_mask mask, int64_t q_offset, const float *sinks, const uint8_t *mask_array,
+                     const int64_t ms[4], bi_dtype dtype, bi_stream_t stream) {
+    if (dtype != BI_BF16 && dtype != BI_F16) return BI_ERR_UNSUPPORTED;
     if (!q || !k || !v || !o || !qs || !ks || !vs || !os) return BI_ERR_INVALID_ARG;
     if (B < 0 || H <= 0 || Hkv <= 0 || Lq < 0 || Lkv < 0 || D <= 0) return BI_ERR_INVALID_ARG;
     if (H % Hkv) return BI_ERR_INVALID_ARG;
-    if (mask != BI_MASK_CAUSAL && mask != BI_MASK_NONE) return BI_ERR_UNSUPPORTED;
+    if (mask != BI_MASK_CAUSAL && mask != BI_MASK_NONE && mask != BI_MASK_ARRAY)
+        return BI_ERR_UNSUPPORTED;
+    if (mask == BI_MASK_ARRAY) {
+        if (!mask_array || !ms || ms[3] != 1) return BI_ERR_INVALID_ARG;
+        for (int i = 0; i < 3; ++i)
+            if (ms[i] < 0) return BI_ERR_INVALID_ARG;
+    } else if (mask_array) {
+        return BI_ERR_INVALID_ARG;
+    }
     if (q_offset < 0) q_offset = Lkv - Lq;
     if (q_offset < 0 || q_offset + Lq > Lkv) return BI_ERR_INVALID_ARG;
     if (Lq == 0 || B == 0) return BI_OK;
@@ -309,6 +317,7 @@ bi_status bi_sdpa(const void *q, const int64_t qs[4], const void *k, const int64
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return BI_ERR_ALIGNMENT;
     for (int i = 0; i < 3; ++i)
         if (qs[i] % 8 || ks[i] % 8 || vs[i] % 8 || os[i] % 8) return BI_ERR_ALIGNMENT;
+    if (sinks && (reinterpret_cast<uintptr_t>(sinks) & 3u)) return BI_ERR_ALIGNMENT;
     if (Lkv > (int64_t(1) << 31) || Lq > (int64_t(1) << 31)) return BI_ERR_UNSUPPORTED;
     bi_status st = check_device();
     if (st != BI_OK) return st;
@@ -317,13 +326,17 @@ bi_status bi_sdpa(const void *q, const int64_t qs[4], const void *k, const int64
     a.B = B; a.H = H; a.Hkv = Hkv; a.Lq = Lq; a.Lkv = Lkv; a.q_offset = q_offset;
     a.group = static_cast<int>(G);
     a.qt = static_cast<int>(128 / G);
-    a.causal = mask == BI_MASK_CAUSAL ? 1 : 0;
+    a.mode = mask == BI_MASK_CAUSAL ? 1 : mask == BI_MASK_ARRAY ? 2 : 0;
     const double sc = scale > 0.0f ? static_cast<double>(scale) : 1.0 / std::sqrt(static_cast<double>(D));
     a.scale_log2 = static_cast<float>(sc * 1.4426950408889634);   // scale * log2(e)
     a.o = o;
     for (int i = 0; i < 4; ++i) a.os[i] = os[i];
     a.err = device_error_word();
     if (!a.err) return BI_ERR_CUDA;
+    a.sinks = sinks;
+    a.mask = mask_array;
+    if (mask == BI_MASK_ARRAY)
+        for (int i = 0; i < 4; ++i) a.ms[i] = ms[i];
 
     CUtensorMap tq, tk, tv;
     {
@@ -349,6 +362,15 @@ bi_status bi_sdpa(const void *q, const int64_t qs[4], const void *k, const int64
         if (st != BI_OK) return st;
     }
     return launch_sdpa(tq, tk, tv, a, dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+bi_status bi_sdpa(const void *q, const int64_t qs[4], const void *k, const int64_t ks[4],
+                  const void *v, const int64_t vs[4], void *o, const int64_t os[4], int64_t B,
+                  int64_t H, int64_t Hkv, int64_t Lq, int64_t Lkv, int64_t D, float scale,
+                  bi_mask mask, int64_t q_offset, bi_dtype dtype, bi_stream_t stream) {
+    if (mask == BI_MASK_ARRAY) return BI_ERR_INVALID_ARG;   // needs the mask: bi_sdpa_ex
+    return bi_sdpa_ex(q, qs, k, ks, v, vs, o, os, B, H, Hkv, Lq, Lkv, D, scale, mask, q_offset,
+                      nullptr, nullptr, nullptr, dtype, stream);
 }
 
 bi_status bi_rmsnorm(const void *x, int64_t ldx, const void *w, void *y, int64_t ldy, int64_t M,

@@ -57,11 +57,14 @@ struct SdpaArgs {
     int64_t B, H, Hkv, Lq, Lkv, q_offset;
     int group;         // H / Hkv
     int qt;            // query positions per tile = 128 / group
-    int causal;
+    int mode;          // 0: no mask, 1: causal, 2: boolean array mask
     float scale_log2;  // scale * log2(e)
     void *o;
     int64_t os[4];
     uint32_t *err;
+    const float *sinks;     // [H] sink logits (units of the scaled scores), or null
+    const uint8_t *mask;    // mode 2: mask[b*ms[0] + h*ms[1] + i*ms[2] + j], nonzero = visible
+    int64_t ms[4];
 };
 bi_status launch_sdpa(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                       const SdpaArgs &args, bi_dtype dt, cudaStream_t s);

@@ -23,7 +23,10 @@
 //   * a chunk that is entirely masked for a row leaves m, l and acc bit-for-bit
 //     unchanged (alpha = 1, p = 0), so extra chunks that a longer query tile
 //     visits, or keys appended beyond a token, change none of its bits;
-//   * o = acc / l (IEEE division), rounded once to the output dtype.
+//   * o = acc / l (IEEE division), rounded once to the output dtype;
+//   * masks: causal (key j visible iff j <= position), none, or a boolean array
+//     mask per (batch, head, query, key); an attention sink (one extra logit
+//     per head, no value) enters as the initial state m = sink * log2 e, l = 1.
 // Every quantity of a row depends only on that row's query, the keys/values,
 // the chunk positions and the row's absolute position -- never on which other
 // rows share the tile.
@@ -97,6 +100,31 @@ __device__ __forceinline__ uint4 pack8x2(const float *v) {
                       cvt2<T>(v[6], v[7]));
 }
 
+// 64 mask bytes (nonzero = visible) starting at p, of which the first `valid`
+// exist (keys past the cache are never visible), as a bit word.
+__device__ __forceinline__ uint64_t mask_bits64(const uint8_t *p, int64_t valid) {
+    uint64_t bits = 0;
+    if (valid >= 64 && (reinterpret_cast<uintptr_t>(p) & 15) == 0) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 w = reinterpret_cast<const uint4 *>(p)[q];
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                // bytes -> 0/1 per byte -> 4 bits (byte b to bit b)
+                const uint32_t ones = __vcmpne4(ws[t], 0u) & 0x01010101u;
+                const uint32_t nib = ((ones * 0x01020408u) >> 24) & 0xFu;
+                bits |= static_cast<uint64_t>(nib) << (16 * q + 4 * t);
+            }
+        }
+    } else {
+        const int n = valid < 0 ? 0 : (valid > 64 ? 64 : static_cast<int>(valid));
+        for (int i = 0; i < n; ++i)
+            if (p[i]) bits |= 1ull << i;
+    }
+    return bits;
+}
+
 // Named barrier shared by the two row warps of one TMEM lane quarter.
 __device__ __forceinline__ void pair_sync(uint32_t quarter) {
     asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
@@ -159,8 +187,8 @@ __global__ void __launch_bounds__(SD_THREADS, 1)
     const int64_t p_lo = tile * Qt;                         // first position of the tile
     int64_t p_max = p_lo + Qt - 1;                          // last valid position in the tile
     if (p_max > q_offset + Lq - 1) p_max = q_offset + Lq - 1;
-    const int nchunks = args.causal ? static_cast<int>(p_max / SD_C + 1)
-                                    : static_cast<int>((Lkv + SD_C - 1) / SD_C);
+    const int nchunks = args.mode == 1 ? static_cast<int>(p_max / SD_C + 1)
+                                       : static_cast<int>((Lkv + SD_C - 1) / SD_C);
 
     if (threadIdx.x == 0) {
         mbar_init(bar_q, 1);
@@ -298,28 +326,47 @@ __global__ void __launch_bounds__(SD_THREADS, 1)
         const bool warp_valid = __any_sync(0xffffffffu, valid) != 0;
         const uint32_t lane_base = (quarter * 32u) << 16;
         const float sl2 = args.scale_log2;
-        // Keys [0, vis_end) are visible to this row.  Rows of the tile that hold no
-        // query of this call compute as if every key were visible; their results
-        // stay in their own rows and are never stored.
-        int64_t vis_end = args.causal ? pos + 1 : Lkv;
+        const int h = kvh * G + g;
+        // Causal / no mask: keys [0, vis_end) are visible to this row.  Rows of the
+        // tile that hold no query of this call compute as if every key were
+        // visible; their results stay in their own rows and are never stored.
+        int64_t vis_end = args.mode == 1 ? pos + 1 : Lkv;
         if (vis_end > Lkv) vis_end = Lkv;
         if (!valid) vis_end = INT64_MAX / 2;
+        // Array mask: this row's mask bytes.
+        const uint8_t *mrow = nullptr;
+        if (args.mode == 2 && valid)
+            mrow = args.mask + b * args.ms[0] + h * args.ms[1] + (pos - q_offset) * args.ms[2];
 
         float acc[64];
 #pragma unroll
         for (int d = 0; d < 64; ++d) acc[d] = 0.0f;
+        // A sink enters as the running state before the first key: m = sink * log2 e,
+        // l = 2^(m - m) = 1, acc = 0.
         float m_run = -INFINITY, l_run = 0.0f, alpha_prev = 1.0f;
+        if (args.sinks) {
+            m_run = __fmul_rn(args.sinks[h], 1.44269504088896341f);
+            l_run = 1.0f;
+        }
 
         for (int j = 0; j <= nchunks; ++j) {
             float alpha = 1.0f;
             if (j < nchunks) {
                 // ---------------- softmax of chunk j over this half's 64 keys
                 const uint32_t sb = j & 1;
+                // Visibility of this half's 64 keys as a bit word (bit i: key0 + i).
+                const int64_t key0 = static_cast<int64_t>(j) * SD_C + half * 64;
+                uint64_t vis;
+                if (mrow) {
+                    vis = mask_bits64(mrow + key0, Lkv - key0);
+                } else {
+                    const int64_t lim64 = vis_end - key0;
+                    const int lim = lim64 < 0 ? 0 : (lim64 > 64 ? 64 : static_cast<int>(lim64));
+                    vis = lim == 64 ? ~0ull : ((1ull << lim) - 1ull);
+                }
+                const bool full = __all_sync(0xffffffffu, vis == ~0ull) != 0;
                 warp_wait(&sfull[sb], (j >> 1) & 1u, abort_flag);
                 tc_fence_after();
-                const int64_t lim64 = vis_end - static_cast<int64_t>(j) * SD_C - half * 64;
-                const int lim = lim64 < 0 ? 0 : (lim64 > 64 ? 64 : static_cast<int>(lim64));
-                const bool full = __all_sync(0xffffffffu, lim == 64) != 0;
                 float x[64];
                 float mloc = -INFINITY;
                 if (warp_valid) {
@@ -338,7 +385,7 @@ __global__ void __launch_bounds__(SD_THREADS, 1)
                     } else {
 #pragma unroll
                         for (int i = 0; i < 64; ++i)
-                            if (i < lim) mloc = fmaxf(mloc, x[i]);
+                            if ((vis >> i) & 1ull) mloc = fmaxf(mloc, x[i]);
                     }
                 }
                 // S(j) is in registers: release its TMEM buffer for S(j+2).
@@ -357,7 +404,7 @@ __global__ void __launch_bounds__(SD_THREADS, 1)
 #pragma unroll
                     for (int i = 0; i < 64; ++i) {
                         float e = ex2_approx(__fmaf_rn(x[i], sl2, -m_new));
-                        if (!full && i >= lim) e = 0.0f;
+                        if (!full && !((vis >> i) & 1ull)) e = 0.0f;
                         x[i] = e;
                         ls4[i & 3] = __fadd_rn(ls4[i & 3], e);
                     }
@@ -409,7 +456,6 @@ __global__ void __launch_bounds__(SD_THREADS, 1)
             alpha_prev = alpha;
         }
         if (valid && !*abort_flag) {
-            const int h = kvh * G + g;
             T *orow = static_cast<T *>(args.o) + b * args.os[0] + h * args.os[1] +
                       (pos - q_offset) * args.os[2] + half * 64;
 #pragma unroll

@@ -46,6 +46,12 @@ def normal(shape, seed: int, std: float = 1.0, dtype="f32", device="cpu") -> tor
     return t.to(dtype_of(dtype))
 
 
+def bernoulli_mask(shape, p_visible: float, seed: int, device="cpu") -> torch.Tensor:
+    """Boolean mask, each element True (visible) with probability ``p_visible``."""
+    g = generator(seed, device)
+    return torch.rand(tuple(shape), generator=g, dtype=torch.float32, device=device) < p_visible
+
+
 def uniform_ids(shape, vocab: int, seed: int, device="cpu") -> torch.Tensor:
     g = generator(seed, device)
     return torch.randint(0, vocab, tuple(shape), generator=g, dtype=torch.int64, device=device)

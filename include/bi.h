@@ -55,7 +55,7 @@ typedef enum {
 
 typedef enum { BI_F32 = 0, BI_F16 = 1, BI_BF16 = 2 } bi_dtype;
 
-typedef enum { BI_MASK_NONE = 0, BI_MASK_CAUSAL = 1 } bi_mask;
+typedef enum { BI_MASK_NONE = 0, BI_MASK_CAUSAL = 1, BI_MASK_ARRAY = 2 } bi_mask;
 
 /* ------------------------------------------------------------------ GEMMs
  * "mlx-batch-invariant" README, "Use" (the op surface) and "How the kernels
@@ -116,6 +116,7 @@ bi_status bi_gemm_config(int64_t N, int64_t K, bi_dtype dtype, int b_layout, int
  *   0 <= q_offset and q_offset + Lq <= Lkv.
  *   mask BI_MASK_CAUSAL: query i sees key j iff j <= q_offset + i.
  *   mask BI_MASK_NONE:   every query sees keys 0..Lkv-1.
+ *   (BI_MASK_ARRAY needs its mask: use bi_sdpa_ex; here it is BI_ERR_INVALID_ARG.)
  *   scale <= 0 selects 1/sqrt(D).
  *   Keys are visited in fixed chunks of 128 at absolute key positions
  *   (0..127, 128..255, ...) in ascending order; queries sit in tiles aligned to
@@ -128,6 +129,25 @@ bi_status bi_sdpa(const void *q, const int64_t qs[4], const void *k, const int64
                   const void *v, const int64_t vs[4], void *o, const int64_t os[4], int64_t B,
                   int64_t H, int64_t Hkv, int64_t Lq, int64_t Lkv, int64_t D, float scale,
                   bi_mask mask, int64_t q_offset, bi_dtype dtype, bi_stream_t stream);
+
+/* Attention with the other two mask forms and attention sinks.
+ * "mlx-batch-invariant" README, "How the kernels work" / Attention ("all three
+ * mask forms") and the paragraph on attention sinks.  Arguments as bi_sdpa, plus:
+ *   mask        BI_MASK_NONE, BI_MASK_CAUSAL, or BI_MASK_ARRAY;
+ *   mask_array  BI_MASK_ARRAY only (else NULL): device uint8, nonzero = visible,
+ *               element (b,h,i,j) at b*ms[0] + h*ms[1] + i*ms[2] + j (ms[3] must
+ *               be 1; a stride of 0 broadcasts).  Keys j >= Lkv are never visible.
+ *   sinks       device fp32 [H] or NULL: one extra logit per query head, in the
+ *               units of the scaled scores, that joins the softmax denominator
+ *               and carries no value; 4-byte aligned.
+ * A query with no visible key and no sink gets NaN.  The mask row of a token
+ * must be the same in every call for its bits to be the same in every call. */
+bi_status bi_sdpa_ex(const void *q, const int64_t qs[4], const void *k, const int64_t ks[4],
+                     const void *v, const int64_t vs[4], void *o, const int64_t os[4], int64_t B,
+                     int64_t H, int64_t Hkv, int64_t Lq, int64_t Lkv, int64_t D, float scale,
+                     bi_mask mask, int64_t q_offset, const float *sinks,
+                     const uint8_t *mask_array, const int64_t ms[4], bi_dtype dtype,
+                     bi_stream_t stream);
 
 /* ------------------------------------------------------------------ decoder glue
  * Row-local ops that a decoder needs around the GEMMs and attention.  The

@@ -99,6 +99,27 @@ def test_sdpa_validation(lib):
                        L.BI_MASK_CAUSAL, -1, L.BI_BF16, s) == L.BI_ERR_INVALID_ARG
 
 
+def test_sdpa_ex_validation(lib):
+    p = ctypes.c_void_p(4096)
+    s = ctypes.c_void_p(0)
+    st4 = L.i64arr([32 * 9 * 128, 9 * 128, 128, 1])
+    ms_ok = L.i64arr([0, 0, 9, 1])
+
+    def call(mask=L.BI_MASK_ARRAY, sinks=None, marr=p, ms=ms_ok):
+        return lib.bi_sdpa_ex(p, st4, p, st4, p, st4, p, st4, 1, 4, 2, 1, 9, 128, 0.0, mask, -1,
+                              sinks, marr, ms, L.BI_BF16, s)
+
+    assert call(marr=None) == L.BI_ERR_INVALID_ARG            # array mode without a mask
+    assert call(ms=None) == L.BI_ERR_INVALID_ARG
+    assert call(ms=L.i64arr([0, 0, 9, 2])) == L.BI_ERR_INVALID_ARG   # last dim not contiguous
+    assert call(ms=L.i64arr([0, -1, 9, 1])) == L.BI_ERR_INVALID_ARG
+    assert call(mask=L.BI_MASK_CAUSAL) == L.BI_ERR_INVALID_ARG        # mask given, mode causal
+    assert call(mask=L.BI_MASK_CAUSAL, marr=None, sinks=ctypes.c_void_p(4098)) == L.BI_ERR_ALIGNMENT
+    # bi_sdpa has no mask argument: the array form is refused there.
+    assert lib.bi_sdpa(p, st4, p, st4, p, st4, p, st4, 1, 4, 2, 1, 9, 128, 0.0,
+                       L.BI_MASK_ARRAY, -1, L.BI_BF16, s) == L.BI_ERR_INVALID_ARG
+
+
 def test_glue_validation(lib):
     p = ctypes.c_void_p(4096)
     s = ctypes.c_void_p(0)
