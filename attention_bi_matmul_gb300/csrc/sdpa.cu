@@ -140,7 +140,9 @@ __device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap *m, int32_t c0
 
 // Registers are granted to warps in groups of four, so a 10-warp block is
 // budgeted as 12 warps: at most 168 registers per thread.
-template <typename T>
+// ARR: the boolean array mask form (the causal and unmasked forms need no mask
+// bytes and keep their visibility as one bound per row).
+template <typename T, bool ARR>
 __global__ void __launch_bounds__(SD_THREADS, 1)
     sdpa_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const SdpaArgs args) {
@@ -335,7 +337,7 @@ __global__ void __launch_bounds__(SD_THREADS, 1)
         if (!valid) vis_end = INT64_MAX / 2;
         // Array mask: this row's mask bytes.
         const uint8_t *mrow = nullptr;
-        if (args.mode == 2 && valid)
+        if (ARR && valid)
             mrow = args.mask + b * args.ms[0] + h * args.ms[1] + (pos - q_offset) * args.ms[2];
 
         float acc[64];
@@ -354,19 +356,20 @@ __global__ void __launch_bounds__(SD_THREADS, 1)
             if (j < nchunks) {
                 // ---------------- softmax of chunk j over this half's 64 keys
                 const uint32_t sb = j & 1;
-                // Visibility of this half's 64 keys as a bit word (bit i: key0 + i).
+                // Visibility of this half's 64 keys key0 + i: bit i of `vis` (array
+                // mask; read before the wait to hide its latency), else i < lim.
                 const int64_t key0 = static_cast<int64_t>(j) * SD_C + half * 64;
-                uint64_t vis;
-                if (mrow) {
-                    vis = mask_bits64(mrow + key0, Lkv - key0);
-                } else {
-                    const int64_t lim64 = vis_end - key0;
-                    const int lim = lim64 < 0 ? 0 : (lim64 > 64 ? 64 : static_cast<int>(lim64));
-                    vis = lim == 64 ? ~0ull : ((1ull << lim) - 1ull);
-                }
-                const bool full = __all_sync(0xffffffffu, vis == ~0ull) != 0;
+                uint64_t vis = ~0ull;
+                if (ARR && mrow) vis = mask_bits64(mrow + key0, Lkv - key0);
                 warp_wait(&sfull[sb], (j >> 1) & 1u, abort_flag);
                 tc_fence_after();
+                int lim = 64;
+                if (!ARR) {
+                    const int64_t lim64 = vis_end - key0;
+                    lim = lim64 < 0 ? 0 : (lim64 > 64 ? 64 : static_cast<int>(lim64));
+                }
+                const bool full =
+                    __all_sync(0xffffffffu, ARR ? vis == ~0ull : lim == 64) != 0;
                 float x[64];
                 float mloc = -INFINITY;
                 if (warp_valid) {
@@ -385,7 +388,7 @@ __global__ void __launch_bounds__(SD_THREADS, 1)
                     } else {
 #pragma unroll
                         for (int i = 0; i < 64; ++i)
-                            if ((vis >> i) & 1ull) mloc = fmaxf(mloc, x[i]);
+                            if (ARR ? ((vis >> i) & 1ull) != 0 : i < lim) mloc = fmaxf(mloc, x[i]);
                     }
                 }
                 // S(j) is in registers: release its TMEM buffer for S(j+2).
@@ -404,7 +407,7 @@ __global__ void __launch_bounds__(SD_THREADS, 1)
 #pragma unroll
                     for (int i = 0; i < 64; ++i) {
                         float e = ex2_approx(__fmaf_rn(x[i], sl2, -m_new));
-                        if (!full && !((vis >> i) & 1ull)) e = 0.0f;
+                        if (!full && (ARR ? ((vis >> i) & 1ull) == 0 : i >= lim)) e = 0.0f;
                         x[i] = e;
                         ls4[i & 3] = __fadd_rn(ls4[i & 3], e);
                     }
@@ -476,7 +479,7 @@ __global__ void __launch_bounds__(SD_THREADS, 1)
     if (threadIdx.x == 0 && *abort_flag) atomicOr(args.err, ERR_TIMEOUT);
 }
 
-template <typename T>
+template <typename T, bool ARR>
 bi_status launch_sdpa_typed(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             const SdpaArgs &args, cudaStream_t s) {
     const int64_t t_first = args.q_offset / args.qt;
@@ -485,7 +488,7 @@ bi_status launch_sdpa_typed(const CUtensorMap &tq, const CUtensorMap &tk, const 
     if (tiles > 0x7fffffff || args.Hkv > 65535 || args.B > 65535) return BI_ERR_UNSUPPORTED;
     dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(args.Hkv),
               static_cast<unsigned>(args.B));
-    sdpa_kernel<T><<<grid, SD_THREADS, SD_SMEM_BYTES, s>>>(tq, tk, tv, args);
+    sdpa_kernel<T, ARR><<<grid, SD_THREADS, SD_SMEM_BYTES, s>>>(tq, tk, tv, args);
     count_launch();
     return cuda_status(cudaGetLastError());
 }
@@ -493,19 +496,27 @@ bi_status launch_sdpa_typed(const CUtensorMap &tq, const CUtensorMap &tk, const 
 }  // namespace
 
 bi_status init_sdpa() {
-    bi_status st = cuda_status(cudaFuncSetAttribute(sdpa_kernel<__nv_bfloat16>,
-                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                    static_cast<int>(SD_SMEM_BYTES)));
-    if (st != BI_OK) return st;
-    return cuda_status(cudaFuncSetAttribute(sdpa_kernel<__half>,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            static_cast<int>(SD_SMEM_BYTES)));
+    void *const fns[] = {reinterpret_cast<void *>(sdpa_kernel<__nv_bfloat16, false>),
+                         reinterpret_cast<void *>(sdpa_kernel<__nv_bfloat16, true>),
+                         reinterpret_cast<void *>(sdpa_kernel<__half, false>),
+                         reinterpret_cast<void *>(sdpa_kernel<__half, true>)};
+    for (void *f : fns) {
+        const bi_status st = cuda_status(cudaFuncSetAttribute(
+            f, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SD_SMEM_BYTES)));
+        if (st != BI_OK) return st;
+    }
+    return BI_OK;
 }
 
 bi_status launch_sdpa(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                       const SdpaArgs &args, bi_dtype dt, cudaStream_t s) {
-    if (dt == BI_BF16) return launch_sdpa_typed<__nv_bfloat16>(tq, tk, tv, args, s);
-    if (dt == BI_F16) return launch_sdpa_typed<__half>(tq, tk, tv, args, s);
+    const bool arr = args.mode == 2;
+    if (dt == BI_BF16)
+        return arr ? launch_sdpa_typed<__nv_bfloat16, true>(tq, tk, tv, args, s)
+                   : launch_sdpa_typed<__nv_bfloat16, false>(tq, tk, tv, args, s);
+    if (dt == BI_F16)
+        return arr ? launch_sdpa_typed<__half, true>(tq, tk, tv, args, s)
+                   : launch_sdpa_typed<__half, false>(tq, tk, tv, args, s);
     return BI_ERR_UNSUPPORTED;
 }
 
