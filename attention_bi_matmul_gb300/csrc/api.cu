@@ -305,10 +305,15 @@ bi_status bi_sdpa_ex(const void *q, const int64_t qs[4], const void *k, const in
     } else if (mask_array) {
         return BI_ERR_INVALID_ARG;
     }
-    if (q_offset < 0) q_offset = Lkv - Lq;
-    if (q_offset < 0 || q_offset + Lq > Lkv) return BI_ERR_INVALID_ARG;
+    // Causal: query i at position q_offset + i must see key 0 and no key past the
+    // cache (q_offset + Lq <= Lkv).  The other forms only use the positions to
+    // align the query tiles; their default is max(Lkv - Lq, 0).
+    if (q_offset < 0)
+        q_offset = mask == BI_MASK_CAUSAL ? Lkv - Lq : (Lkv > Lq ? Lkv - Lq : 0);
+    if (q_offset < 0 || (mask == BI_MASK_CAUSAL && q_offset + Lq > Lkv)) return BI_ERR_INVALID_ARG;
     if (Lq == 0 || B == 0) return BI_OK;
-    if (D != 128) return BI_ERR_UNSUPPORTED;
+    if (Lkv == 0) return BI_ERR_INVALID_ARG;   // no key at all
+    if (D != 64 && D != 96 && D != 128) return BI_ERR_UNSUPPORTED;
     const int64_t G = H / Hkv;
     if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return BI_ERR_UNSUPPORTED;
     if (qs[3] != 1 || ks[3] != 1 || vs[3] != 1 || os[3] != 1) return BI_ERR_INVALID_ARG;
@@ -318,7 +323,7 @@ bi_status bi_sdpa_ex(const void *q, const int64_t qs[4], const void *k, const in
     for (int i = 0; i < 3; ++i)
         if (qs[i] % 8 || ks[i] % 8 || vs[i] % 8 || os[i] % 8) return BI_ERR_ALIGNMENT;
     if (sinks && (reinterpret_cast<uintptr_t>(sinks) & 3u)) return BI_ERR_ALIGNMENT;
-    if (Lkv > (int64_t(1) << 31) || Lq > (int64_t(1) << 31)) return BI_ERR_UNSUPPORTED;
+    if (Lkv > (int64_t(1) << 31) || q_offset + Lq > (int64_t(1) << 31)) return BI_ERR_UNSUPPORTED;
     bi_status st = check_device();
     if (st != BI_OK) return st;
 
@@ -326,6 +331,8 @@ bi_status bi_sdpa_ex(const void *q, const int64_t qs[4], const void *k, const in
     a.B = B; a.H = H; a.Hkv = Hkv; a.Lq = Lq; a.Lkv = Lkv; a.q_offset = q_offset;
     a.group = static_cast<int>(G);
     a.qt = static_cast<int>(128 / G);
+    a.D = static_cast<int>(D);
+    a.dp = D <= 64 ? 64 : 128;
     a.mode = mask == BI_MASK_CAUSAL ? 1 : mask == BI_MASK_ARRAY ? 2 : 0;
     const double sc = scale > 0.0f ? static_cast<double>(scale) : 1.0 / std::sqrt(static_cast<double>(D));
     a.scale_log2 = static_cast<float>(sc * 1.4426950408889634);   // scale * log2(e)

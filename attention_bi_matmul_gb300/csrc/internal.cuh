@@ -57,6 +57,8 @@ struct SdpaArgs {
     int64_t B, H, Hkv, Lq, Lkv, q_offset;
     int group;         // H / Hkv
     int qt;            // query positions per tile = 128 / group
+    int D;             // head dim (64, 96 or 128)
+    int dp;            // D padded to whole 64-element panels: 64 or 128
     int mode;          // 0: no mask, 1: causal, 2: boolean array mask
     float scale_log2;  // scale * log2(e)
     void *o;

@@ -52,7 +52,6 @@ namespace bi {
 
 namespace {
 
-constexpr int SD_D = 128;       // head dim
 constexpr int SD_C = 128;       // keys per chunk
 constexpr int SD_ROWS = 128;    // rows per query tile
 constexpr int SD_KST = 2;       // K ring depth
@@ -60,23 +59,30 @@ constexpr int SD_VST = 2;       // V ring depth
 constexpr int SD_PF = 2;        // chunks prefetched into L2 beyond the rings
 constexpr int SD_THREADS = 320;
 constexpr uint32_t SD_PANEL = SD_ROWS * 128;        // 16 KB: 128 rows x 64 elements
-constexpr uint32_t SD_TILE = 2 * SD_PANEL;          // 32 KB: 128 rows x 128 elements
-constexpr uint32_t SD_TMEM_COLS = 512;              // S0 S1 O0 O1, 128 columns each
+constexpr uint32_t SD_PTILE = 2 * SD_PANEL;         // P: 128 rows x 128 keys
+constexpr uint32_t SD_TMEM_COLS = 512;              // S0 S1 (128 columns each), O0 O1 (DP each)
 
+// DP: the head dim padded to whole 64-element panels (64 or 128).  Head dims
+// that are not a multiple of 64 are loaded with the TMA's zero fill past D, so
+// the padded columns add exact zeros to Q K^T and produce O columns that are
+// never stored.
+template <int DP>
 struct SdSmem {
+    static constexpr uint32_t NP = DP / 64;                      // panels per Q/K/V tile
+    static constexpr uint32_t TILE = NP * SD_PANEL;              // 128 rows x DP elements
     // byte offsets from the 1024-aligned base
     static constexpr uint32_t Q = 0;
-    static constexpr uint32_t K = Q + SD_TILE;
-    static constexpr uint32_t V = K + SD_KST * SD_TILE;
-    static constexpr uint32_t P = V + SD_VST * SD_TILE;
-    static constexpr uint32_t MX = P + SD_TILE;                  // float[2][128] half maxima
+    static constexpr uint32_t K = Q + TILE;
+    static constexpr uint32_t V = K + SD_KST * TILE;
+    static constexpr uint32_t P = V + SD_VST * TILE;
+    static constexpr uint32_t MX = P + SD_PTILE;                 // float[2][128] half maxima
     static constexpr uint32_t LS = MX + 2 * 128 * 4;             // float[2][128] half sums
     static constexpr uint32_t BARS = LS + 2 * 128 * 4;           // uint64 barriers
     static constexpr uint32_t NBARS = 1 + 2 * SD_KST + 2 * SD_VST + 4 + 2 + 4 + 1;
     static constexpr uint32_t MISC = BARS + NBARS * 8;           // tmem slot, abort flag
     static constexpr uint32_t END = MISC + 16;
+    static constexpr size_t BYTES = 1024 + END;
 };
-constexpr size_t SD_SMEM_BYTES = 1024 + SdSmem::END;
 
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
@@ -141,13 +147,17 @@ __device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap *m, int32_t c0
 // Registers are granted to warps in groups of four, so a 10-warp block is
 // budgeted as 12 warps: at most 168 registers per thread.
 // ARR: the boolean array mask form (the causal and unmasked forms need no mask
-// bytes and keep their visibility as one bound per row).
-template <typename T, bool ARR>
+// bytes and keep their visibility as one bound per row).  DP: padded head dim.
+template <typename T, bool ARR, int DP>
 __global__ void __launch_bounds__(SD_THREADS, 1)
     sdpa_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const SdpaArgs args) {
+    using SdSmem = bi::SdSmem<DP>;
+    constexpr uint32_t NP = SdSmem::NP;
+    constexpr uint32_t SD_TILE = SdSmem::TILE;
+    constexpr int DH = DP / 2;                 // output columns per row warp
     constexpr uint32_t IDESC_S = mma_idesc(IsBf16<T>::value, SD_ROWS, SD_C, false);
-    constexpr uint32_t IDESC_PV = mma_idesc(IsBf16<T>::value, SD_ROWS, SD_D, true);
+    constexpr uint32_t IDESC_PV = mma_idesc(IsBf16<T>::value, SD_ROWS, DP, true);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -225,13 +235,15 @@ __global__ void __launch_bounds__(SD_THREADS, 1)
             prefetch_tmap(&tmV);
             const int32_t qi0 = static_cast<int32_t>(p_lo - q_offset);  // may be negative
             mbar_arrive_expect_tx(bar_q, SD_TILE);
-            tma_load_4d(sQ, &tmQ, bar_q, 0, kvh * G, qi0, b);
-            tma_load_4d(sQ + SD_PANEL, &tmQ, bar_q, 64, kvh * G, qi0, b);
+#pragma unroll
+            for (uint32_t pn = 0; pn < NP; ++pn)
+                tma_load_4d(sQ + pn * SD_PANEL, &tmQ, bar_q, 64 * pn, kvh * G, qi0, b);
             for (int j = SD_KST; j < SD_KST + SD_PF && j < nchunks; ++j) {
-                tma_prefetch_4d(&tmK, 0, j * SD_C, kvh, b);
-                tma_prefetch_4d(&tmK, 64, j * SD_C, kvh, b);
-                tma_prefetch_4d(&tmV, 0, j * SD_C, kvh, b);
-                tma_prefetch_4d(&tmV, 64, j * SD_C, kvh, b);
+#pragma unroll
+                for (uint32_t pn = 0; pn < NP; ++pn) {
+                    tma_prefetch_4d(&tmK, 64 * pn, j * SD_C, kvh, b);
+                    tma_prefetch_4d(&tmV, 64 * pn, j * SD_C, kvh, b);
+                }
             }
             int armed = 0;
             bool ok = true;
@@ -239,20 +251,25 @@ __global__ void __launch_bounds__(SD_THREADS, 1)
                 const uint32_t sk = j % SD_KST, phk = (j / SD_KST) & 1u;
                 if (!mbar_wait(&kempty[sk], phk ^ 1u, abort_flag)) { ok = false; break; }
                 mbar_arrive_expect_tx(&kfull[sk], SD_TILE);
-                tma_load_4d(sK + sk * SD_TILE, &tmK, &kfull[sk], 0, j * SD_C, kvh, b);
-                tma_load_4d(sK + sk * SD_TILE + SD_PANEL, &tmK, &kfull[sk], 64, j * SD_C, kvh, b);
+#pragma unroll
+                for (uint32_t pn = 0; pn < NP; ++pn)
+                    tma_load_4d(sK + sk * SD_TILE + pn * SD_PANEL, &tmK, &kfull[sk], 64 * pn,
+                                j * SD_C, kvh, b);
                 const uint32_t sv = j % SD_VST, phv = (j / SD_VST) & 1u;
                 if (!mbar_wait(&vempty[sv], phv ^ 1u, abort_flag)) { ok = false; armed = 2 * j + 1; break; }
                 mbar_arrive_expect_tx(&vfull[sv], SD_TILE);
-                tma_load_4d(sV + sv * SD_TILE, &tmV, &vfull[sv], 0, j * SD_C, kvh, b);
-                tma_load_4d(sV + sv * SD_TILE + SD_PANEL, &tmV, &vfull[sv], 64, j * SD_C, kvh, b);
+#pragma unroll
+                for (uint32_t pn = 0; pn < NP; ++pn)
+                    tma_load_4d(sV + sv * SD_TILE + pn * SD_PANEL, &tmV, &vfull[sv], 64 * pn,
+                                j * SD_C, kvh, b);
                 armed = 2 * j + 2;
                 const int jp = j + SD_KST + SD_PF;   // next chunk not yet asked for
                 if (jp < nchunks) {
-                    tma_prefetch_4d(&tmK, 0, jp * SD_C, kvh, b);
-                    tma_prefetch_4d(&tmK, 64, jp * SD_C, kvh, b);
-                    tma_prefetch_4d(&tmV, 0, jp * SD_C, kvh, b);
-                    tma_prefetch_4d(&tmV, 64, jp * SD_C, kvh, b);
+#pragma unroll
+                    for (uint32_t pn = 0; pn < NP; ++pn) {
+                        tma_prefetch_4d(&tmK, 64 * pn, jp * SD_C, kvh, b);
+                        tma_prefetch_4d(&tmV, 64 * pn, jp * SD_C, kvh, b);
+                    }
                 }
             }
             if (!ok) {
@@ -281,7 +298,7 @@ __global__ void __launch_bounds__(SD_THREADS, 1)
                     tc_fence_after();
                     const uint32_t k_addr = smem_u32(sK + sk * SD_TILE);
 #pragma unroll
-                    for (int kk = 0; kk < SD_D / 16; ++kk) {
+                    for (int kk = 0; kk < DP / 16; ++kk) {
                         const uint32_t off = (kk >> 2) * SD_PANEL + (kk & 3) * 32;
                         mma_f16_ss(tmem_base + sb * 128, smem_desc(q_addr + off, 16, 1024),
                                    smem_desc(k_addr + off, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
@@ -302,7 +319,7 @@ __global__ void __launch_bounds__(SD_THREADS, 1)
 #pragma unroll
                     for (int kk = 0; kk < SD_C / 16; ++kk) {
                         const uint32_t aoff = (kk >> 2) * SD_PANEL + (kk & 3) * 32;
-                        mma_f16_ss(tmem_base + 256 + ob * 128, smem_desc(p_addr + aoff, 16, 1024),
+                        mma_f16_ss(tmem_base + 256 + ob * DP, smem_desc(p_addr + aoff, 16, 1024),
                                    smem_desc(v_addr + kk * 2048, SD_PANEL, 1024), IDESC_PV,
                                    kk > 0 ? 1u : 0u);
                     }
@@ -320,7 +337,7 @@ __global__ void __launch_bounds__(SD_THREADS, 1)
         // aborting) only turns the remaining work into no-ops, so the two warps of
         // a lane quarter always meet at the same named barriers.
         const uint32_t quarter = static_cast<uint32_t>(warp & 3);
-        const int half = (warp - 2) >> 2;                    // 0: keys/dims 0..63, 1: 64..127
+        const int half = (warp - 2) >> 2;  // keys 64*half..+63; output dims DH*half..+DH-1
         const int r = static_cast<int>(quarter) * 32 + lane; // tile row == TMEM lane
         const int qi = r / G, g = r - (r / G) * G;
         const int64_t pos = p_lo + qi;
@@ -340,9 +357,9 @@ __global__ void __launch_bounds__(SD_THREADS, 1)
         if (ARR && valid)
             mrow = args.mask + b * args.ms[0] + h * args.ms[1] + (pos - q_offset) * args.ms[2];
 
-        float acc[64];
+        float acc[DH];
 #pragma unroll
-        for (int d = 0; d < 64; ++d) acc[d] = 0.0f;
+        for (int d = 0; d < DH; ++d) acc[d] = 0.0f;
         // A sink enters as the running state before the first key: m = sink * log2 e,
         // l = 2^(m - m) = 1, acc = 0.
         float m_run = -INFINITY, l_run = 0.0f, alpha_prev = 1.0f;
@@ -440,16 +457,25 @@ __global__ void __launch_bounds__(SD_THREADS, 1)
                 warp_wait(&ofull[ob], (i >> 1) & 1u, abort_flag);
                 tc_fence_after();
                 if (warp_valid) {
-                    uint32_t o0[32], o1[32];
-                    const uint32_t o_addr = tmem_base + lane_base + 256 + ob * 128 + half * 64;
-                    tmem_ld32(o_addr, o0);
-                    tmem_ld32(o_addr + 32, o1);
-                    tmem_wait_ld(o0);
-                    tmem_wait_ld(o1);
+                    const uint32_t o_addr = tmem_base + lane_base + 256 + ob * DP + half * DH;
+                    if constexpr (DH == 64) {
+                        uint32_t o0[32], o1[32];
+                        tmem_ld32(o_addr, o0);
+                        tmem_ld32(o_addr + 32, o1);
+                        tmem_wait_ld(o0);
+                        tmem_wait_ld(o1);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        acc[e] = __fmaf_rn(acc[e], alpha_prev, __uint_as_float(o0[e]));
-                        acc[32 + e] = __fmaf_rn(acc[32 + e], alpha_prev, __uint_as_float(o1[e]));
+                        for (int e = 0; e < 32; ++e) {
+                            acc[e] = __fmaf_rn(acc[e], alpha_prev, __uint_as_float(o0[e]));
+                            acc[32 + e] = __fmaf_rn(acc[32 + e], alpha_prev, __uint_as_float(o1[e]));
+                        }
+                    } else {
+                        uint32_t o0[32];
+                        tmem_ld32(o_addr, o0);
+                        tmem_wait_ld(o0);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            acc[e] = __fmaf_rn(acc[e], alpha_prev, __uint_as_float(o0[e]));
                     }
                 }
                 tc_fence_before();
@@ -460,9 +486,10 @@ __global__ void __launch_bounds__(SD_THREADS, 1)
         }
         if (valid && !*abort_flag) {
             T *orow = static_cast<T *>(args.o) + b * args.os[0] + h * args.os[1] +
-                      (pos - q_offset) * args.os[2] + half * 64;
+                      (pos - q_offset) * args.os[2] + half * DH;
 #pragma unroll
-            for (int d8 = 0; d8 < 8; ++d8) {
+            for (int d8 = 0; d8 < DH / 8; ++d8) {
+                if (half * DH + d8 * 8 >= args.D) break;   // padded columns past the head dim
                 float v[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) v[e] = __fdiv_rn(acc[d8 * 8 + e], l_run);
@@ -479,7 +506,7 @@ __global__ void __launch_bounds__(SD_THREADS, 1)
     if (threadIdx.x == 0 && *abort_flag) atomicOr(args.err, ERR_TIMEOUT);
 }
 
-template <typename T, bool ARR>
+template <typename T, bool ARR, int DP>
 bi_status launch_sdpa_typed(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             const SdpaArgs &args, cudaStream_t s) {
     const int64_t t_first = args.q_offset / args.qt;
@@ -488,21 +515,43 @@ bi_status launch_sdpa_typed(const CUtensorMap &tq, const CUtensorMap &tk, const 
     if (tiles > 0x7fffffff || args.Hkv > 65535 || args.B > 65535) return BI_ERR_UNSUPPORTED;
     dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(args.Hkv),
               static_cast<unsigned>(args.B));
-    sdpa_kernel<T, ARR><<<grid, SD_THREADS, SD_SMEM_BYTES, s>>>(tq, tk, tv, args);
+    sdpa_kernel<T, ARR, DP><<<grid, SD_THREADS, SdSmem<DP>::BYTES, s>>>(tq, tk, tv, args);
     count_launch();
     return cuda_status(cudaGetLastError());
 }
 
 }  // namespace
 
+namespace {
+template <typename T, bool ARR, int DP>
+bi_status set_smem_attr() {
+    return cuda_status(cudaFuncSetAttribute(sdpa_kernel<T, ARR, DP>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            static_cast<int>(SdSmem<DP>::BYTES)));
+}
+template <typename T, int DP>
+bi_status dispatch_mask(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                        const SdpaArgs &args, cudaStream_t s) {
+    return args.mode == 2 ? launch_sdpa_typed<T, true, DP>(tq, tk, tv, args, s)
+                          : launch_sdpa_typed<T, false, DP>(tq, tk, tv, args, s);
+}
+template <typename T>
+bi_status dispatch_dp(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                      const SdpaArgs &args, cudaStream_t s) {
+    if (args.dp == 64) return dispatch_mask<T, 64>(tq, tk, tv, args, s);
+    if (args.dp == 128) return dispatch_mask<T, 128>(tq, tk, tv, args, s);
+    return BI_ERR_UNSUPPORTED;
+}
+}  // namespace
+
 bi_status init_sdpa() {
-    void *const fns[] = {reinterpret_cast<void *>(sdpa_kernel<__nv_bfloat16, false>),
-                         reinterpret_cast<void *>(sdpa_kernel<__nv_bfloat16, true>),
-                         reinterpret_cast<void *>(sdpa_kernel<__half, false>),
-                         reinterpret_cast<void *>(sdpa_kernel<__half, true>)};
-    for (void *f : fns) {
-        const bi_status st = cuda_status(cudaFuncSetAttribute(
-            f, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SD_SMEM_BYTES)));
+    bi_status (*const fns[])() = {
+        set_smem_attr<__nv_bfloat16, false, 64>, set_smem_attr<__nv_bfloat16, true, 64>,
+        set_smem_attr<__nv_bfloat16, false, 128>, set_smem_attr<__nv_bfloat16, true, 128>,
+        set_smem_attr<__half, false, 64>,        set_smem_attr<__half, true, 64>,
+        set_smem_attr<__half, false, 128>,       set_smem_attr<__half, true, 128>};
+    for (auto f : fns) {
+        const bi_status st = f();
         if (st != BI_OK) return st;
     }
     return BI_OK;
@@ -510,13 +559,8 @@ bi_status init_sdpa() {
 
 bi_status launch_sdpa(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                       const SdpaArgs &args, bi_dtype dt, cudaStream_t s) {
-    const bool arr = args.mode == 2;
-    if (dt == BI_BF16)
-        return arr ? launch_sdpa_typed<__nv_bfloat16, true>(tq, tk, tv, args, s)
-                   : launch_sdpa_typed<__nv_bfloat16, false>(tq, tk, tv, args, s);
-    if (dt == BI_F16)
-        return arr ? launch_sdpa_typed<__half, true>(tq, tk, tv, args, s)
-                   : launch_sdpa_typed<__half, false>(tq, tk, tv, args, s);
+    if (dt == BI_BF16) return dispatch_dp<__nv_bfloat16>(tq, tk, tv, args, s);
+    if (dt == BI_F16) return dispatch_dp<__half>(tq, tk, tv, args, s);
     return BI_ERR_UNSUPPORTED;
 }
 

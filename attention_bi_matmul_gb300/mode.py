@@ -47,7 +47,7 @@ def batch_invariant_mode(strict: bool = True):
         if _gemm_ok(input, weight) and (bias is None or bias.is_contiguous()):
             try:
                 return api.linear(input, weight, bias)
-            except ValueError:
+            except (ValueError, api.L.BiError):
                 pass
         return fallback("linear%s" % (tuple(input.shape),), orig["linear"], input, weight, bias)
 
@@ -55,7 +55,13 @@ def batch_invariant_mode(strict: bool = True):
         if out is None and _gemm_ok(a, b):
             try:
                 return api.matmul(a, b)
-            except ValueError:
+            except (ValueError, api.L.BiError):
+                pass
+        elif out is None and b.dim() == 2 and b.stride(0) == 1 and _gemm_ok(a, b.t()):
+            # a @ w.t() with w[N, K] contiguous: the nn.Linear layout.
+            try:
+                return api.linear(a, b.t())
+            except (ValueError, api.L.BiError):
                 pass
         return fallback("matmul%s@%s" % (tuple(a.shape), tuple(b.shape)), orig["matmul"], a, b,
                         **({} if out is None else {"out": out}))
@@ -67,18 +73,22 @@ def batch_invariant_mode(strict: bool = True):
         if out is None and _gemm_ok(mat1, mat2) and mat1.dim() == 2:
             try:
                 return api.addmm(input, mat1, mat2, alpha=float(alpha), beta=float(beta))
-            except ValueError:
+            except (ValueError, api.L.BiError):
                 pass
         return fallback("addmm", orig["addmm"], input, mat1, mat2, beta=beta, alpha=alpha,
                         **({} if out is None else {"out": out}))
 
     def _sdpa(query, key, value, attn_mask=None, dropout_p=0.0, is_causal=False, scale=None,
               enable_gqa=False):
-        ok = (attn_mask is None and dropout_p == 0.0 and query.dim() == 4 and query.is_cuda
-              and query.dtype in (torch.float16, torch.bfloat16)
+        bool_mask = attn_mask is not None and attn_mask.dtype == torch.bool and not is_causal
+        ok = ((attn_mask is None or bool_mask) and dropout_p == 0.0 and query.dim() == 4
+              and query.is_cuda and query.dtype in (torch.float16, torch.bfloat16)
               and (enable_gqa or key.shape[1] == query.shape[1]))
         if ok:
             try:
+                if bool_mask:
+                    # torch's boolean mask: True = the key takes part, as the array form.
+                    return api.sdpa(query, key, value, mask=attn_mask, scale=scale)
                 # torch's is_causal aligns the mask to the top-left corner: query i sees keys <= i.
                 return api.sdpa(query, key, value, causal=bool(is_causal),
                                 q_offset=0 if is_causal else None, scale=scale)

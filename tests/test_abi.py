@@ -91,7 +91,13 @@ def test_sdpa_validation(lib):
     assert call(Lq=10) == L.BI_ERR_INVALID_ARG                # default offset negative
     assert call(mask=5) == L.BI_ERR_UNSUPPORTED
     assert call(dt=L.BI_F32) == L.BI_ERR_UNSUPPORTED
-    assert call(D=64) == L.BI_ERR_UNSUPPORTED                 # head dim not built
+    assert call(D=80) == L.BI_ERR_UNSUPPORTED                 # head dim not built
+    assert call(D=256) == L.BI_ERR_UNSUPPORTED
+    assert call(D=32) == L.BI_ERR_UNSUPPORTED
+    # Without the causal rule the positions only align the tiles: more queries than
+    # keys pass validation; no keys at all do not.
+    assert call(Lq=10, mask=L.BI_MASK_NONE) != L.BI_ERR_INVALID_ARG
+    assert call(Lkv=0, q_offset=0, mask=L.BI_MASK_NONE) == L.BI_ERR_INVALID_ARG
     assert call(H=64, Hkv=2) == L.BI_ERR_UNSUPPORTED          # group of 32 not built
     assert call(Lq=0) == L.BI_OK                              # empty: no-op
     bad = L.i64arr([32 * 9 * 128, 9 * 128, 128, 2])
