@@ -116,8 +116,92 @@ def linear(x: torch.Tensor, w: torch.Tensor, bias: torch.Tensor | None = None,
     return y.view(*lead, N) if out is None and y.is_contiguous() else (y if out is None else out)
 
 
+def _entry_stride(t: torch.Tensor, nlead: int) -> int | None:
+    """One element stride that walks the first `nlead` dims of t in order, or None."""
+    if nlead == 0:
+        return 0
+    sizes, strides = t.shape[:nlead], t.stride()[:nlead]
+    live = [(n, st) for n, st in zip(sizes, strides) if n != 1]
+    if not live:
+        return 0
+    if all(st == 0 for _, st in live):
+        return 0
+    for (n0, st0), (n1, st1) in zip(live, live[1:]):
+        if st0 != st1 * n1:
+            return None
+    return live[-1][1]
+
+
+def bmm(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """Stacked matmul a[..., M, K] . b[..., K, N] with broadcast leading dims.
+
+    b may be any view whose last two dims are either [K, N] with N contiguous or
+    the transpose of an [N, K] block with K contiguous (``w.transpose(-1, -2)``).
+    Each entry's bits equal those of the unbatched call on that entry.
+    """
+    dev = _cuda(a, b, out)
+    if a.dim() < 2 or b.dim() < 2 or a.shape[-1] != b.shape[-2] or a.dtype != b.dtype:
+        raise ValueError("bmm: a[..., M, K] and b[..., K, N] of one dtype")
+    M, K = a.shape[-2:]
+    N = b.shape[-1]
+    lead = tuple(torch.broadcast_shapes(a.shape[:-2], b.shape[:-2]))
+    nl = len(lead)
+    ae = a.expand(*lead, M, K)
+    be = b.expand(*lead, K, N)
+    r8 = lambda n: (n + 7) // 8 * 8
+    if out is None:
+        # 16-bit rows padded to a multiple of 8 elements (16 bytes) when needed
+        Np = N if (a.dtype == torch.float32 or N % 8 == 0) else r8(N)
+        y = torch.empty((*lead, M, Np), dtype=a.dtype, device=a.device)[..., :N]
+    else:
+        y = out
+    if tuple(y.shape) != (*lead, M, N) or y.stride(-1) != 1:
+        raise ValueError("bmm: out must be [..., M, N] with N contiguous")
+    # b's layout: [K, N] with N contiguous (1), or the transpose of [N, K] with K
+    # contiguous (0).  The row stride of a single row is never used; it gets the
+    # smallest aligned value.
+    if N > 1 and be.stride(-1) == 1:
+        layout, ldb = 1, (be.stride(-2) if K > 1 else r8(N))
+    elif K > 1 and be.stride(-2) == 1:
+        layout, ldb = 0, (be.stride(-1) if N > 1 else r8(K))
+    elif N == 1 and K == 1:
+        layout, ldb = 1, 8
+    elif N == 1:
+        layout, ldb = 1, be.stride(-2)
+    elif K == 1:
+        layout, ldb = 0, be.stride(-1)
+    else:
+        raise ValueError("bmm: b needs N or K contiguous")
+    if ae.stride(-1) != 1 and K > 1:
+        raise ValueError("bmm: a's last dimension must be contiguous")
+    sa, sb, sy = _entry_stride(ae, nl), _entry_stride(be, nl), _entry_stride(y, nl)
+    if sa is None or sb is None or sy is None:
+        # No single stride walks the leading dims (e.g. b[3,K,N] broadcast to
+        # [2,3,K,N]): one launch per index of the first leading dim.  Entries are
+        # independent, so this changes no bit.
+        if nl < 2:
+            raise ValueError("bmm: leading dimensions cannot be walked with one stride")
+        for i in range(lead[0]):
+            bmm(ae[i], be[i], out=y[i])
+        return y
+    batch = 1
+    for n in lead:
+        batch *= n
+    lda = ae.stride(-2) if M > 1 else r8(K)
+    ldy = y.stride(-2) if M > 1 else r8(N)
+    if batch == 0 or M == 0:
+        return y
+    with _On(dev) as s:
+        L.check(L.load().bi_matmul_batched(_p(ae), lda, sa, _p(be), ldb, sb, layout, _p(y), ldy,
+                                           sy, batch, M, N, K, _dt(a), s), "bi_matmul_batched")
+    return y
+
+
 def matmul(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
-    """y = a . b with b[K, N] (N contiguous); leading dims of a are batch."""
+    """y = a . b with b[K, N] (N contiguous); leading dims of a are batch.  A b with
+    leading dims of its own is a stacked matmul (``bmm``)."""
+    if b.dim() > 2:
+        return bmm(a, b, out)
     dev = _cuda(a, b, out)
     lead = a.shape[:-1]
     a2 = _rows(a, "a")

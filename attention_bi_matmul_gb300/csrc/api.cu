@@ -242,7 +242,7 @@ bi_status bi_linear(const void *x, int64_t ldx, const void *w, int64_t ldw, cons
     bi_status st = check_gemm(x, ldx, w, ldw, y, ldy, M, N, K, dtype, true);
     if (st != BI_OK) return st;
     GemmArgs args{};
-    args.M = M; args.N = N; args.K = K; args.y = y; args.ldy = ldy;
+    args.M = M; args.N = N; args.K = K; args.y = y; args.ldy = ldy; args.batch = 1;
     args.bias = bias;
     args.epi = bias ? EPI_BIAS : EPI_NONE;
     return run_gemm(x, ldx, w, ldw, true, args, dtype, reinterpret_cast<cudaStream_t>(stream));
@@ -253,9 +253,30 @@ bi_status bi_matmul(const void *a, int64_t lda, const void *b, int64_t ldb, void
     bi_status st = check_gemm(a, lda, b, ldb, y, ldy, M, N, K, dtype, false);
     if (st != BI_OK) return st;
     GemmArgs args{};
-    args.M = M; args.N = N; args.K = K; args.y = y; args.ldy = ldy;
+    args.M = M; args.N = N; args.K = K; args.y = y; args.ldy = ldy; args.batch = 1;
     args.epi = EPI_NONE;
     return run_gemm(a, lda, b, ldb, false, args, dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+bi_status bi_matmul_batched(const void *a, int64_t lda, int64_t sa, const void *b, int64_t ldb,
+                            int64_t sb, int b_layout, void *y, int64_t ldy, int64_t sy,
+                            int64_t batch, int64_t M, int64_t N, int64_t K, bi_dtype dtype,
+                            bi_stream_t stream) {
+    if (b_layout != 0 && b_layout != 1) return BI_ERR_INVALID_ARG;
+    const bool b_nk = b_layout == 0;
+    bi_status st = check_gemm(a, lda, b, ldb, y, ldy, M, N, K, dtype, b_nk);
+    if (st != BI_OK) return st;
+    if (batch < 0 || sa < 0 || sb < 0 || sy < 0) return BI_ERR_INVALID_ARG;
+    if (batch == 0 || M == 0) return BI_OK;
+    // Entries of y must not overlap (each is written by its own tiles).
+    if (batch > 1 && sy < (M - 1) * ldy + N) return BI_ERR_INVALID_ARG;
+    if (batch > 65535) return BI_ERR_UNSUPPORTED;
+    if (dtype != BI_F32 && (sa % 8 || sb % 8 || sy % 8)) return BI_ERR_ALIGNMENT;
+    GemmArgs args{};
+    args.M = M; args.N = N; args.K = K; args.y = y; args.ldy = ldy;
+    args.batch = batch; args.sa = sa; args.sb = sb; args.sy = sy;
+    args.epi = EPI_NONE;
+    return run_gemm(a, lda, b, ldb, b_nk, args, dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 
 bi_status bi_addmm(const void *c, int64_t ldc, const void *a, int64_t lda, const void *b,
@@ -266,7 +287,7 @@ bi_status bi_addmm(const void *c, int64_t ldc, const void *a, int64_t lda, const
     if (!c || ldc < 0 || (ldc > 0 && ldc < N)) return BI_ERR_INVALID_ARG;
     if (!std::isfinite(alpha) || !std::isfinite(beta)) return BI_ERR_INVALID_ARG;
     GemmArgs args{};
-    args.M = M; args.N = N; args.K = K; args.y = y; args.ldy = ldy;
+    args.M = M; args.N = N; args.K = K; args.y = y; args.ldy = ldy; args.batch = 1;
     args.c = c; args.ldc = ldc; args.alpha = alpha; args.beta = beta;
     args.epi = EPI_ADDMM;
     return run_gemm(a, lda, b, ldb, false, args, dtype, reinterpret_cast<cudaStream_t>(stream));

@@ -26,6 +26,9 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(const float *__restrict__
     __shared__ float As[F_BK][F_BM + 4];
     __shared__ float Bs[F_BK][F_BN + 4];
     const int64_t M = args.M, N = args.N, K = args.K;
+    const int64_t e = blockIdx.z;                  // batch entry
+    a += e * args.sa;
+    b += e * args.sb;
     const int64_t m0 = static_cast<int64_t>(blockIdx.y) * F_BM;
     const int64_t n0 = static_cast<int64_t>(blockIdx.x) * F_BN;
     const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
@@ -71,7 +74,7 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(const float *__restrict__
 
     // Epilogue, fixed order in fp32 (same rule as the tensor-core path):
     //   bias:  y = acc + bias[n];   addmm: y = (alpha * acc) + (beta * c).
-    float *y = static_cast<float *>(args.y);
+    float *y = static_cast<float *>(args.y) + e * args.sy;
 #pragma unroll
     for (int i = 0; i < F_TM; ++i) {
         const int64_t m = m0 + ty * F_TM + i;
@@ -99,8 +102,9 @@ bi_status launch_gemm_f32(const float *a, int64_t lda, const float *b, int64_t l
                           const GemmArgs &args, cudaStream_t s) {
     const int64_t gx = (args.N + F_BN - 1) / F_BN;
     const int64_t gy = (args.M + F_BM - 1) / F_BM;
-    if (gx > 0x7fffffff || gy > 65535) return BI_ERR_UNSUPPORTED;
-    dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
+    if (gx > 0x7fffffff || gy > 65535 || args.batch > 65535) return BI_ERR_UNSUPPORTED;
+    dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy),
+              static_cast<unsigned>(args.batch));
     if (b_nk)
         gemm_f32_kernel<true><<<grid, 256, 0, s>>>(a, lda, b, ldb, args);
     else

@@ -69,10 +69,10 @@ __device__ __forceinline__ uint4 pack8(const float *v) {
     return p.u;
 }
 
-// Epilogue of 32 consecutive output columns [n0, n0+32) of row m.
+// Epilogue of 32 consecutive output columns [n0, n0+32) of row m of batch entry e.
 template <typename T>
-__device__ __forceinline__ void gemm_epilogue32(const uint32_t (&r)[32], int64_t m, int64_t n0,
-                                                const GemmArgs &a) {
+__device__ __forceinline__ void gemm_epilogue32(const uint32_t (&r)[32], int64_t e, int64_t m,
+                                                int64_t n0, const GemmArgs &a) {
     float v[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
@@ -89,7 +89,7 @@ __device__ __forceinline__ void gemm_epilogue32(const uint32_t (&r)[32], int64_t
             if (n0 + i < N)
                 v[i] = __fadd_rn(__fmul_rn(a.alpha, v[i]), __fmul_rn(a.beta, to_f32<T>(crow[n0 + i])));
     }
-    T *yrow = static_cast<T *>(a.y) + m * a.ldy;
+    T *yrow = static_cast<T *>(a.y) + e * a.sy + m * a.ldy;
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
         const int64_t n = n0 + 8 * g;
@@ -128,9 +128,13 @@ __host__ __device__ constexpr size_t tc_smem_bytes() {
            256 /* barriers etc */;
 }
 
-// Tile t -> (m block, n block), grouped so that concurrently running tiles share A and B in L2.
+// Tile t -> (batch entry, m block, n block); within an entry, tiles are grouped so
+// that concurrently running tiles share A and B in L2.
 __device__ __forceinline__ void tc_tile_coords(int64_t t, int64_t num_m, int64_t num_n,
-                                               int64_t &mb, int64_t &nb) {
+                                               int64_t &e, int64_t &mb, int64_t &nb) {
+    const int64_t per_entry = num_m * num_n;
+    e = t / per_entry;
+    t -= e * per_entry;
     const int64_t in_group = (int64_t)TC_GROUP_M * num_n;
     const int64_t g = t / in_group;
     const int64_t first_m = g * TC_GROUP_M;
@@ -173,7 +177,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int64_t M = args.M, N = args.N, K = args.K;
     const int64_t num_m = (M + TC_BM - 1) / TC_BM;
     const int64_t num_n = (N + BN - 1) / BN;
-    const int64_t total = num_m * num_n;
+    const int64_t total = args.batch * num_m * num_n;
     const int KB = static_cast<int>((K + KP * TC_BK - 1) / (KP * TC_BK));   // stages per tile
 
     if (threadIdx.x == 0) {
@@ -209,24 +213,28 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             uint32_t it = 0, s = 0, ph = 0;
             bool ok = true;
             for (int64_t t = blockIdx.x; ok && t < total; t += gridDim.x) {
-                int64_t mb, nb;
-                tc_tile_coords(t, num_m, num_n, mb, nb);
+                int64_t e, mb, nb;
+                tc_tile_coords(t, num_m, num_n, e, mb, nb);
+                // A shared operand is a tensor map with one batch entry.
+                const int32_t ea = args.sa ? static_cast<int32_t>(e) : 0;
+                const int32_t eb = args.sb ? static_cast<int32_t>(e) : 0;
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
                     mbar_arrive_expect_tx(&full[s], tx);
 #pragma unroll
                     for (int p = 0; p < KP; ++p) {
                         const int32_t k0 = (kb * KP + p) * TC_BK;   // beyond K: zero-filled
-                        tma_load_2d(sA + s * A_BYTES + p * A_PANEL, &tmA, &full[s], k0,
-                                    static_cast<int32_t>(mb * TC_BM));
+                        tma_load_3d(sA + s * A_BYTES + p * A_PANEL, &tmA, &full[s], k0,
+                                    static_cast<int32_t>(mb * TC_BM), ea);
                         if (!B_MN) {
-                            tma_load_2d(sB + s * B_BYTES + p * B_PANEL, &tmB, &full[s], k0,
-                                        static_cast<int32_t>(nb * BN));
+                            tma_load_3d(sB + s * B_BYTES + p * B_PANEL, &tmB, &full[s], k0,
+                                        static_cast<int32_t>(nb * BN), eb);
                         } else {
 #pragma unroll
                             for (int j = 0; j < BN / 64; ++j)
-                                tma_load_2d(sB + s * B_BYTES + p * B_PANEL + j * 8192, &tmB,
-                                            &full[s], static_cast<int32_t>(nb * BN + j * 64), k0);
+                                tma_load_3d(sB + s * B_BYTES + p * B_PANEL + j * 8192, &tmB,
+                                            &full[s], static_cast<int32_t>(nb * BN + j * 64), k0,
+                                            eb);
                         }
                     }
                     // 128-column tiles stream their weight panels from HBM with a short
@@ -238,11 +246,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         for (int p = 0; p < KP; ++p) {
                             const int32_t kq = ((kb + STAGES) * KP + p) * TC_BK;
                             if (!B_MN) {
-                                tma_prefetch_2d(&tmB, kq, static_cast<int32_t>(nb * BN));
+                                tma_prefetch_3d(&tmB, kq, static_cast<int32_t>(nb * BN), eb);
                             } else {
 #pragma unroll
                                 for (int j = 0; j < BN / 64; ++j)
-                                    tma_prefetch_2d(&tmB, static_cast<int32_t>(nb * BN + j * 64), kq);
+                                    tma_prefetch_3d(&tmB, static_cast<int32_t>(nb * BN + j * 64),
+                                                    kq, eb);
                             }
                         }
                     }
@@ -304,8 +313,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int row_in_tile = static_cast<int>(quarter) * 32 + lane;
         uint32_t tc = 0;
         for (int64_t t = blockIdx.x; t < total; t += gridDim.x, ++tc) {
-            int64_t mb, nb;
-            tc_tile_coords(t, num_m, num_n, mb, nb);
+            int64_t e, mb, nb;
+            tc_tile_coords(t, num_m, num_n, e, mb, nb);
             const uint32_t acc = tc & 1u;
             const uint32_t aph = (tc >> 1) & 1u;
             if (!warp_wait(&tfull[acc], aph, abort_flag)) break;
@@ -316,7 +325,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 uint32_t r[32];
                 tmem_ld32(tmem_base + ((quarter * 32u) << 16) + acc * BN + cc * 32, r);
                 tmem_wait_ld(r);
-                if (m < M) gemm_epilogue32<T>(r, m, nb * BN + cc * 32, args);
+                if (m < M) gemm_epilogue32<T>(r, e, m, nb * BN + cc * 32, args);
             }
             tc_fence_before();
             __syncwarp();
@@ -355,7 +364,8 @@ bi_status launch_tc_inst(const CUtensorMap &ta, const CUtensorMap &tb, const Gem
                          int stages_req, cudaStream_t s) {
     (void)stages_req;
     constexpr size_t SMEM = tc_smem_bytes<BN>();
-    const int64_t tiles = ((args.M + TC_BM - 1) / TC_BM) * ((args.N + BN - 1) / BN);
+    const int64_t tiles =
+        args.batch * ((args.M + TC_BM - 1) / TC_BM) * ((args.N + BN - 1) / BN);
     const int sms = device_sm_count();
     const int grid = static_cast<int>(tiles < sms ? tiles : sms);
     gemm_tc_kernel<T, BN, B_MN><<<grid, TC_THREADS, SMEM, s>>>(ta, tb, args);
@@ -371,24 +381,27 @@ bi_status launch_gemm_tc_typed(const void *a, int64_t lda, const void *b, int64_
                                cudaStream_t s) {
     const int BN = cfg.block_n;
     CUtensorMap ta, tb;
+    // Third dimension: the batch entry.  A shared operand (batch stride 0) gets one
+    // entry, with the packed stride standing in for the unused one.
     {
-        const uint64_t dims[2] = {static_cast<uint64_t>(args.K), static_cast<uint64_t>(args.M)};
-        const uint64_t strides[1] = {static_cast<uint64_t>(lda) * 2};
-        const uint32_t box[2] = {TC_BK, static_cast<uint32_t>(args.a_rows)};
-        bi_status st = encode_tmap(&ta, dt, 2, const_cast<void *>(a), dims, strides, box, true);
+        const uint64_t ea = args.sa ? static_cast<uint64_t>(args.batch) : 1;
+        const uint64_t dims[3] = {static_cast<uint64_t>(args.K), static_cast<uint64_t>(args.M), ea};
+        const uint64_t strides[2] = {static_cast<uint64_t>(lda) * 2,
+                                     static_cast<uint64_t>(args.sa ? args.sa : lda * args.M) * 2};
+        const uint32_t box[3] = {TC_BK, static_cast<uint32_t>(args.a_rows), 1};
+        bi_status st = encode_tmap(&ta, dt, 3, const_cast<void *>(a), dims, strides, box, true);
         if (st != BI_OK) return st;
     }
-    if (b_nk) {
-        const uint64_t dims[2] = {static_cast<uint64_t>(args.K), static_cast<uint64_t>(args.N)};
-        const uint64_t strides[1] = {static_cast<uint64_t>(ldb) * 2};
-        const uint32_t box[2] = {TC_BK, static_cast<uint32_t>(BN)};
-        bi_status st = encode_tmap(&tb, dt, 2, const_cast<void *>(b), dims, strides, box, true);
-        if (st != BI_OK) return st;
-    } else {
-        const uint64_t dims[2] = {static_cast<uint64_t>(args.N), static_cast<uint64_t>(args.K)};
-        const uint64_t strides[1] = {static_cast<uint64_t>(ldb) * 2};
-        const uint32_t box[2] = {64, TC_BK};
-        bi_status st = encode_tmap(&tb, dt, 2, const_cast<void *>(b), dims, strides, box, true);
+    {
+        const uint64_t eb = args.sb ? static_cast<uint64_t>(args.batch) : 1;
+        const uint64_t inner = b_nk ? args.K : args.N, outer = b_nk ? args.N : args.K;
+        const uint64_t dims[3] = {inner, outer, eb};
+        const uint64_t strides[2] = {static_cast<uint64_t>(ldb) * 2,
+                                     static_cast<uint64_t>(args.sb ? args.sb : ldb * outer) * 2};
+        const uint32_t box[3] = {b_nk ? static_cast<uint32_t>(TC_BK) : 64u,
+                                 b_nk ? static_cast<uint32_t>(BN) : static_cast<uint32_t>(TC_BK),
+                                 1};
+        bi_status st = encode_tmap(&tb, dt, 3, const_cast<void *>(b), dims, strides, box, true);
         if (st != BI_OK) return st;
     }
     if (b_nk) {

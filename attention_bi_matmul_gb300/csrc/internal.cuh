@@ -24,6 +24,11 @@ struct GemmArgs {
     int epi;
     uint32_t *err;     // device error word
     int a_rows;        // rows of A each copy moves: min(128, M rounded up to 16)
+    // Batched calls: `batch` independent problems of the same shape (1 otherwise).
+    // Entry e reads a + e*sa and b + e*sb and writes y + e*sy (elements); a stride
+    // of 0 shares that operand across the batch.
+    int64_t batch;
+    int64_t sa, sb, sy;
 };
 
 // Tile configuration of the tensor-core GEMM for one (N, K, dtype, layout).

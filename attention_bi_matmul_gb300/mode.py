@@ -28,7 +28,8 @@ def _gemm_ok(a: torch.Tensor, b: torch.Tensor) -> bool:
 @contextlib.contextmanager
 def batch_invariant_mode(strict: bool = True):
     """Patch torch.matmul, Tensor.__matmul__, torch.addmm, F.linear and
-    F.scaled_dot_product_attention for the duration of the block."""
+    F.scaled_dot_product_attention for the duration of the block.  matmul of
+    stacked operands ([..., M, K] @ [..., K, N]) runs the batched GEMM."""
     orig = {
         "matmul": torch.matmul,
         "tmatmul": torch.Tensor.__matmul__,
@@ -52,7 +53,14 @@ def batch_invariant_mode(strict: bool = True):
         return fallback("linear%s" % (tuple(input.shape),), orig["linear"], input, weight, bias)
 
     def _matmul(a, b, *, out=None):
-        if out is None and _gemm_ok(a, b):
+        if (out is None and b.dim() >= 3 and a.dim() >= 2 and a.is_cuda and b.is_cuda
+                and a.dtype in _DTYPES and b.dtype == a.dtype):
+            # stacked operands: one batched launch, each entry as the plain GEMM
+            try:
+                return api.bmm(a, b)
+            except (ValueError, api.L.BiError):
+                pass
+        elif out is None and _gemm_ok(a, b):
             try:
                 return api.matmul(a, b)
             except (ValueError, api.L.BiError):

@@ -94,6 +94,27 @@ bi_status bi_addmm(const void *c, int64_t ldc, const void *a, int64_t lda, const
                    int64_t ldb, void *y, int64_t ldy, int64_t M, int64_t N, int64_t K,
                    float alpha, float beta, bi_dtype dtype, bi_stream_t stream);
 
+/* Batched matmul: `batch` independent problems of one shape,
+ *   y_e[M,N] = a_e[M,K] . b_e,   e = 0 .. batch-1,
+ * with a_e = a + e*sa, b_e = b + e*sb, y_e = y + e*sy (element offsets).
+ * "mlx-batch-invariant" README, "Use": matmul is one of the routed ops, and a
+ * framework matmul also takes stacked operands [..., M, K] @ [..., K, N] (a
+ * reading: the page does not discuss them).  Each entry is the GEMM above.
+ *   b_layout 1: b_e is [K,N] with row stride ldb (N contiguous), as bi_matmul;
+ *   b_layout 0: b_e is [N,K] with row stride ldb (K contiguous), y_e = a_e . b_e^T
+ *               (torch.matmul(a, w.transpose(-1, -2)) for a contiguous w).
+ *   sa or sb may be 0: that operand is shared by every entry.  Entries of y must
+ *   not overlap: sy >= (M-1)*ldy + N when batch > 1.  16-bit dtypes: sa, sb, sy
+ *   multiples of 8 elements.  batch <= 65535.
+ * The tile configuration is that of the unbatched call for (N, K, dtype,
+ * b_layout), and every entry's bits equal those of bi_matmul (b_layout 1) or
+ * bi_linear without bias (b_layout 0) on that entry alone: an entry's result
+ * depends neither on the batch size nor on the other entries. */
+bi_status bi_matmul_batched(const void *a, int64_t lda, int64_t sa, const void *b, int64_t ldb,
+                            int64_t sb, int b_layout, void *y, int64_t ldy, int64_t sy,
+                            int64_t batch, int64_t M, int64_t N, int64_t K, bi_dtype dtype,
+                            bi_stream_t stream);
+
 /* Reports the tile configuration the GEMM entry points use for (N, K, dtype,
  * weight layout).  b_layout: 0 = linear (w[N,K]), 1 = matmul/addmm (b[K,N]).
  * Outputs (each may be NULL): block_n = output columns per tile, stages =

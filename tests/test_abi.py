@@ -74,6 +74,25 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.bi_linear(p, 8, p, 8, nul, p, 8, 0, 8, 8, L.BI_BF16, s) == L.BI_OK
 
 
+def test_matmul_batched_validation(lib):
+    p = ctypes.c_void_p(4096)
+    s = ctypes.c_void_p(0)
+
+    def call(sa=64 * 64, sb=64 * 64, sy=64 * 64, batch=3, layout=1, dt=L.BI_BF16, M=64):
+        return lib.bi_matmul_batched(p, 64, sa, p, 64, sb, layout, p, 64, sy, batch, M, 64, 64,
+                                     dt, s)
+
+    assert call(layout=2) == L.BI_ERR_INVALID_ARG
+    assert call(batch=-1) == L.BI_ERR_INVALID_ARG
+    assert call(sa=-8) == L.BI_ERR_INVALID_ARG
+    assert call(sy=63 * 64) == L.BI_ERR_INVALID_ARG           # entries of y overlap
+    assert call(sa=12) == L.BI_ERR_ALIGNMENT                   # 16-bit: multiples of 8
+    assert call(batch=70000) == L.BI_ERR_UNSUPPORTED
+    assert call(batch=0) == L.BI_OK                            # empty: no-op
+    assert call(M=0) == L.BI_OK
+    assert call(sa=12, dt=L.BI_F32) != L.BI_ERR_ALIGNMENT      # fp32 takes any stride
+
+
 def test_sdpa_validation(lib):
     p = ctypes.c_void_p(4096)
     s = ctypes.c_void_p(0)

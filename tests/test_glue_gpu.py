@@ -113,6 +113,6 @@ def test_python_errors(bi):
         bi.linear(x[:, 1:], w[:, 1:])      # misaligned row start -> BI_ERR_ALIGNMENT
     with pytest.raises(ValueError):
         bi.linear(x.cpu(), w.cpu())
-    q = torch.zeros((1, 4, 1, 64), dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros((1, 4, 1, 80), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(bi.BiError):
-        bi.sdpa(q, q[:, :1], q[:, :1])     # head dim 64 not built
+        bi.sdpa(q, q[:, :1], q[:, :1])     # head dim 80 not built
