@@ -12,7 +12,8 @@ Two sources, both seeded:
 
 Distributions follow the workloads in the design notes: GEMM operands
 N(0,1)/sqrt(K) (fp32 linear: N(0,1)/16, bias N(0,0.1)), attention q/k/v N(0,1),
-decoder weights N(0,0.02), token ids uniform over the vocabulary.
+decoder weights N(0,0.02), token ids uniform over the vocabulary, quantized
+weights as uniformly random packed words with per-group scales and biases.
 """
 from __future__ import annotations
 
@@ -89,6 +90,27 @@ def gemm16(M: int, N: int, K: int, dtype="bf16", seed: int = 0, layout="matmul",
         return a, b
     c = normal((N,) if c_row else (M, N), seed + 2, s, dtype, device)
     return a, b, c
+
+
+def qweights(N: int, K: int, bits: int, group_size: int, dtype="bf16", seed: int = 0,
+             device="cpu"):
+    """Synthetic group-wise affine quantized weights of an [N, K] layer.
+
+    wq: int32 [N, K*bits/32], uniformly random words (every bit pattern is a valid
+    packing of 32/bits fields); scales ~ U(0.5, 1.5) * 6 sigma / (2^bits - 1) and
+    biases ~ -3 sigma * U(0.8, 1.2) per group, sigma = 1/sqrt(K), so the weights
+    span about [-3 sigma, 3 sigma] as a quantized N(0, sigma^2) layer would.
+    """
+    g = generator(seed, device)
+    wq = torch.randint(-2 ** 31, 2 ** 31, (N, K * bits // 32), generator=g, dtype=torch.int64,
+                       device=device).to(torch.int32)
+    sigma = 1.0 / math.sqrt(K)
+    G = K // group_size
+    u = torch.rand((N, G), generator=g, dtype=torch.float32, device=device)
+    scales = (0.5 + u) * (6.0 * sigma / (2 ** bits - 1))
+    v = torch.rand((N, G), generator=g, dtype=torch.float32, device=device)
+    biases = -3.0 * sigma * (0.8 + 0.4 * v)
+    return wq, scales.to(dtype_of(dtype)), biases.to(dtype_of(dtype))
 
 
 def sdpa_qkv(B: int, H: int, Hkv: int, Lq: int, Lkv: int, D: int = 128, dtype="bf16",

@@ -74,6 +74,8 @@ class Oracle:
         lib.oracle_sdpa_ex.argtypes = [_I64, _I64, _I64, _I64, _I64, _I64, _D, _D, _D,
                                        ctypes.c_double, ctypes.c_int, _I64, _D,
                                        ctypes.POINTER(ctypes.c_ubyte), _D, _D]
+        lib.oracle_qlinear.argtypes = [_I64, _I64, _I64, _D, ctypes.POINTER(ctypes.c_uint32),
+                                       _I64, _D, _D, _I64, ctypes.c_int, _I64, _D, _D, _D]
         lib.oracle_rmsnorm.argtypes = [_I64, _I64, _D, _D, ctypes.c_double, _D]
         lib.oracle_rope.argtypes = [_I64, _I64, _I64, _D, ctypes.POINTER(ctypes.c_int64),
                                     ctypes.c_double, _D]
@@ -162,6 +164,25 @@ class Oracle:
                                 _p(o), _p(nrm))
         return o, nrm
 
+    def qlinear(self, x, wq, scales, biases, bits, group_size, bias=None):
+        """Group-wise affine quantized linear: x[M,K], wq uint32 [N, K*bits/32] (packed
+        along K, lowest field first), scales/biases [N, K/group_size]; y = x . w^T + bias."""
+        x, scales, biases = _f64(x), _f64(scales), _f64(biases)
+        if hasattr(wq, "detach"):
+            wq = wq.detach().to("cpu").numpy()
+        wq = np.ascontiguousarray(np.asarray(wq).view(np.uint32))
+        bias = None if bias is None else _f64(bias)
+        M, K = x.shape
+        N = wq.shape[0]
+        assert bits in (2, 4, 8) and K % group_size == 0 and K * bits % 32 == 0
+        assert wq.shape == (N, K * bits // 32) and scales.shape == (N, K // group_size)
+        assert biases.shape == scales.shape and (bias is None or bias.shape == (N,))
+        y = np.empty((M, N)); nrm = np.empty((M, N))
+        self.lib.oracle_qlinear(M, N, K, _p(x), wq.ctypes.data_as(ctypes.POINTER(ctypes.c_uint32)),
+                                wq.shape[1], _p(scales), _p(biases), scales.shape[1], int(bits),
+                                int(group_size), _p(bias), _p(y), _p(nrm))
+        return y, nrm
+
     def rmsnorm(self, x, w, eps=1e-6):
         """y = x / sqrt(mean(x^2) + eps) * w over the last dim; x[M,N], w[N]."""
         x, w = _f64(x), _f64(w)
@@ -224,6 +245,10 @@ def sdpa(q, k, v, causal=True, q_offset=None, scale=None):
 
 def sdpa_ex(q, k, v, causal=True, q_offset=None, scale=None, sinks=None, mask=None):
     return default().sdpa_ex(q, k, v, causal, q_offset, scale, sinks, mask)
+
+
+def qlinear(x, wq, scales, biases, bits, group_size, bias=None):
+    return default().qlinear(x, wq, scales, biases, bits, group_size, bias)
 
 
 def rmsnorm(x, w, eps=1e-6):

@@ -30,7 +30,11 @@
  *   - SwiGLU: input [M, 2I] = [gate | up], y = silu(gate) * up;
  *   - array mask: boolean, nonzero = the key is visible;
  *   - attention sink: one extra logit per query head, in the units of the
- *     scaled scores, that joins the softmax denominator with no value.
+ *     scaled scores, that joins the softmax denominator with no value;
+ *   - quantized weights ("Quantized models": 2, 4 and 8-bit affine, group-wise):
+ *     w[n,k] = scales[n, k/gs] * q[n,k] + biases[n, k/gs], with q the unsigned
+ *     `bits`-wide field number (k mod 32/bits) of the 32-bit word k / (32/bits)
+ *     of row n, fields numbered from the least significant bit.
  * Every function also returns the per-element normaliser that the tolerance
  * is stated against (the sum of the magnitudes of the terms).
  *
@@ -208,6 +212,46 @@ void oracle_sdpa(int64_t B, int64_t H, int64_t Hkv, int64_t Lq, int64_t Lkv, int
                  int causal, int64_t q_offset, double *o, double *nrm)
 {
     oracle_sdpa_ex(B, H, Hkv, Lq, Lkv, D, q, k, v, scale, causal, q_offset, 0, 0, o, nrm);
+}
+
+/* Quantized linear ("mlx-batch-invariant" README, "Quantized models"):
+ *   q[n,k]  = (wq[n*ldq + k/f] >> (bits * (k mod f))) & (2^bits - 1),  f = 32/bits
+ *   w[n,k]  = scales[n*ldsb + k/gs] * q[n,k] + biases[n*ldsb + k/gs]
+ *   y[m,n]  = sum_k x[m,k] * w[n,k]  (+ bias[n]);   nrm = sum_k |x w| (+ |bias|)
+ * w is formed exactly in fp64 (no rounding to a 16-bit type).               */
+void oracle_qlinear(int64_t M, int64_t N, int64_t K, const double *x, const uint32_t *wq,
+                    int64_t ldq, const double *scales, const double *biases, int64_t ldsb,
+                    int bits, int64_t gs, const double *bias, double *y, double *nrm)
+{
+    const int64_t f = 32 / bits;
+    const uint32_t fmask = bits == 32 ? 0xFFFFFFFFu : ((1u << bits) - 1u);
+#pragma omp parallel
+    {
+        double *wrow = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+#pragma omp for schedule(static)
+        for (int64_t n = 0; n < N; ++n) {
+            for (int64_t k = 0; k < K; ++k) {
+                const uint32_t word = wq[n * ldq + k / f];
+                const uint32_t q = (word >> (bits * (k % f))) & fmask;
+                wrow[k] = scales[n * ldsb + k / gs] * (double)q + biases[n * ldsb + k / gs];
+            }
+            for (int64_t m = 0; m < M; ++m) {
+                double acc = 0.0, mag = 0.0;
+                for (int64_t k = 0; k < K; ++k) {
+                    double t = x[m * K + k] * wrow[k];
+                    acc += t;
+                    mag += fabs(t);
+                }
+                if (bias) {
+                    acc += bias[n];
+                    mag += fabs(bias[n]);
+                }
+                y[m * N + n] = acc;
+                if (nrm) nrm[m * N + n] = mag;
+            }
+        }
+        free(wrow);
+    }
 }
 
 /* RMSNorm over the last dim: y[m,n] = x[m,n] / sqrt(mean_n x[m,.]^2 + eps) * w[n] */

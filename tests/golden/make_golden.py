@@ -44,6 +44,15 @@ def main():
              "and 'How the kernels work' / Attention",
         inputs=dict(q=_l(q), k=_l(k), v=_l(v), causal=True, q_offset=3), o=o.tolist(),
         nrm=nrm.tolist())
+    x = synth.normal((3, 64), 10, 1.0, "bf16")
+    wq, sc, bi = synth.qweights(5, 64, 4, 32, "bf16", seed=11)
+    bias = synth.normal((5,), 12, 0.1, "bf16")
+    y, nrm = oracle.qlinear(x, wq, sc, bi, 4, 32, bias)
+    fixtures["qlinear_4bit_small"] = dict(
+        cite="mlx-batch-invariant README, 'Quantized models' (2, 4 and 8-bit affine weights "
+             "unpacked inside the K loop)",
+        inputs=dict(x=_l(x), wq=wq.tolist(), scales=_l(sc), biases=_l(bi), bias=_l(bias),
+                    bits=4, group_size=32), y=y.tolist(), nrm=nrm.tolist())
     for name, fx in fixtures.items():
         with open(os.path.join(HERE, name + ".json"), "w") as f:
             json.dump(fx, f, indent=1)

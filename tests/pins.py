@@ -380,9 +380,114 @@ def pin_swiglu(O):
     assert np.array_equal(O.swiglu(gu0), np.zeros((4, 24))), "silu(0) == 0"
 
 
+# ------------------------------------------------------------------ quantized linear pins
+
+def _fields_by_bitstring(words, bits):
+    """Unpack uint32 words into `bits`-wide fields, least significant first, by reading
+    each word's binary string (a method independent of shifts and masks)."""
+    out = []
+    for w in np.asarray(words, dtype=np.uint64).ravel():
+        s = format(int(w), "032b")[::-1]           # s[i] = bit i
+        for j in range(32 // bits):
+            out.append(int(s[j * bits:(j + 1) * bits][::-1], 2))
+    return out
+
+
+def _fields_by_unpackbits(wq, bits):
+    """[N, W] uint32 -> [N, W*32/bits] fields, via numpy's little-endian bit unpacking."""
+    b = np.unpackbits(np.ascontiguousarray(wq, dtype="<u4").view(np.uint8), axis=1,
+                      bitorder="little").astype(np.int64)
+    b = b.reshape(wq.shape[0], -1, bits)
+    return (b * (1 << np.arange(bits))).sum(axis=2)
+
+
+def _qweights(rng, N, K, bits, gs, full_range=True):
+    wq = rng.integers(0, 2 ** 32, size=(N, K * bits // 32), dtype=np.uint64).astype(np.uint32)
+    scales = np.abs(_fp32_vals(rng, (N, K // gs), 0.1)) + 0.01
+    biases = _fp32_vals(rng, (N, K // gs), 0.5)
+    return wq, scales, biases
+
+
+def pin_qlinear_bruteforce(O):
+    """qlinear == exact rational sum over the bit-string unpacking, within (K+1)*u*nrm."""
+    rng = _rng(41)
+    for bits in (2, 4, 8):
+        for gs in (32, 64):
+            M, N, K = 2, 3, 128
+            wq, sc, bi = _qweights(rng, N, K, bits, gs)
+            x = _fp32_vals(rng, (M, K))
+            bias = _fp32_vals(rng, (N,))
+            y, nrm = O.qlinear(x, wq, sc, bi, bits, gs, bias)
+            for n in range(N):
+                q = _fields_by_bitstring(wq[n], bits)
+                w = [Fraction(sc[n, k // gs]) * q[k] + Fraction(bi[n, k // gs]) for k in range(K)]
+                for m in range(M):
+                    exact = sum(Fraction(x[m, k]) * w[k] for k in range(K)) + Fraction(bias[n])
+                    mag = sum(abs(Fraction(x[m, k]) * w[k]) for k in range(K)) + abs(Fraction(bias[n]))
+                    bound = (K + 2) * U64 * float(mag)
+                    assert abs(y[m, n] - float(exact)) <= bound, ("qlinear", bits, gs, m, n)
+                    assert abs(nrm[m, n] - float(mag)) <= bound, ("qlinear nrm", bits, gs, m, n)
+
+
+def pin_qlinear_integer_exact(O):
+    """Integer scales, biases and activations: every term and sum is an exact integer, so
+    y equals an int64 matmul over numpy's bit unpacking exactly."""
+    rng = _rng(42)
+    for bits in (2, 4, 8):
+        for gs in (32, 128):
+            M, N, K = 3, 5, 256
+            wq = rng.integers(0, 2 ** 32, size=(N, K * bits // 32), dtype=np.uint64).astype(np.uint32)
+            sc = rng.integers(1, 4, size=(N, K // gs)).astype(np.float64)
+            bi = rng.integers(-8, 8, size=(N, K // gs)).astype(np.float64)
+            x = rng.integers(-2, 3, size=(M, K))
+            q = _fields_by_unpackbits(wq, bits)
+            w = q * np.repeat(sc, gs, axis=1).astype(np.int64) + np.repeat(bi, gs, axis=1).astype(np.int64)
+            want = x @ w.T
+            y, _ = O.qlinear(x.astype(np.float64), wq, sc, bi, bits, gs)
+            assert np.array_equal(y, want.astype(np.float64)), ("qlinear integer", bits, gs)
+
+
+def pin_qlinear_closed_forms(O):
+    """All fields 0: w = the group's bias; all fields 2^bits - 1: w = s (2^bits - 1) + b."""
+    rng = _rng(43)
+    M, N, K, gs = 2, 4, 192, 64
+    x = _fp32_vals(rng, (M, K))
+    for bits in (2, 4, 8):
+        _, sc, bi = _qweights(rng, N, K, bits, gs)
+        for fill, qv in ((0, 0), (0xFFFFFFFF, 2 ** bits - 1)):
+            wq = np.full((N, K * bits // 32), fill, dtype=np.uint32)
+            y, _ = O.qlinear(x, wq, sc, bi, bits, gs)
+            w = np.repeat(sc * qv + bi, gs, axis=1)
+            want = np.array([[math.fsum(x[m] * w[n]) for n in range(N)] for m in range(M)])
+            _close(y, want, 4 * K * U64 * (np.abs(x) @ np.abs(w).T), "qlinear closed form %d" % bits)
+
+
+def pin_qlinear_group_locality(O):
+    """With x zero outside group g, y depends on group g's scale and bias only."""
+    rng = _rng(44)
+    M, N, K, gs, bits = 2, 3, 256, 64, 4
+    wq, sc, bi = _qweights(rng, N, K, bits, gs)
+    for g in range(K // gs):
+        x = np.zeros((M, K))
+        x[:, g * gs:(g + 1) * gs] = _fp32_vals(rng, (M, gs))
+        y0, _ = O.qlinear(x, wq, sc, bi, bits, gs)
+        sc2, bi2 = sc.copy(), bi.copy()
+        others = [h for h in range(K // gs) if h != g]
+        sc2[:, others] *= 3.0
+        bi2[:, others] += 1.0
+        y1, _ = O.qlinear(x, wq, sc2, bi2, bits, gs)
+        assert np.array_equal(y0, y1), ("group locality", g)
+        sc3 = sc.copy()
+        sc3[:, g] *= 2.0
+        y2, _ = O.qlinear(x, wq, sc3, bi, bits, gs)
+        assert not np.array_equal(y0, y2), ("group's own scale matters", g)
+
+
 ALL_PINS = [pin_linear_bruteforce, pin_matmul_bruteforce, pin_addmm_bruteforce,
             pin_gemm_integer_exact, pin_gemm_numpy, pin_gemm_identities,
             pin_sdpa_bruteforce, pin_sdpa_torch, pin_sdpa_closed_forms, pin_sdpa_structure,
             pin_sdpa_sinks_and_masks_bruteforce, pin_sdpa_sinks_and_masks_torch,
             pin_sdpa_mask_structure,
+            pin_qlinear_bruteforce, pin_qlinear_integer_exact, pin_qlinear_closed_forms,
+            pin_qlinear_group_locality,
             pin_rmsnorm, pin_rope, pin_swiglu]

@@ -48,3 +48,12 @@ def test_sdpa_fixture():
 def test_fixtures_cite_the_page():
     for name in ("linear_f32_small", "addmm_bf16_small", "sdpa_causal_gqa_small"):
         assert "mlx-batch-invariant README" in _load(name)["cite"]
+
+
+def test_qlinear_fixture():
+    fx = _load("qlinear_4bit_small")
+    i = fx["inputs"]
+    wq = np.asarray(i["wq"], dtype=np.int64).astype(np.int32).view(np.uint32)
+    y, nrm = oracle.qlinear(i["x"], wq, i["scales"], i["biases"], i["bits"], i["group_size"],
+                            i["bias"])
+    _close(y, fx["y"]); _close(nrm, fx["nrm"])

@@ -30,6 +30,15 @@ MUTATIONS = {
     "sdpa_exp_sign": ("s[j] = exp(s[j] - mx);", "s[j] = exp(mx - s[j]);"),
     "sdpa_no_scale": ("s[j] = scale * t;", "s[j] = t;"),
     "sdpa_normaliser": ("r += p * fabs(vb[j * D + d]);", "r += fabs(vb[j * D + d]);"),
+    "qlinear_field_order": ("const uint32_t q = (word >> (bits * (k % f))) & fmask;",
+                            "const uint32_t q = (word >> (bits * (f - 1 - k % f))) & fmask;"),
+    "qlinear_group_index": ("wrow[k] = scales[n * ldsb + k / gs] * (double)q",
+                            "wrow[k] = scales[n * ldsb + (k % gs) % ldsb] * (double)q"),
+    "qlinear_scale_bias_swapped": (
+        "scales[n * ldsb + k / gs] * (double)q + biases[n * ldsb + k / gs]",
+        "biases[n * ldsb + k / gs] * (double)q + scales[n * ldsb + k / gs]"),
+    "qlinear_signed_fields": ("* (double)q + biases", "* ((double)q - (double)(fmask >> 1)) + biases"),
+    "qlinear_drops_bias": ("acc += bias[n];", ";"),
     "rmsnorm_sum_not_mean": ("sqrt(ss / (double)N + eps)", "sqrt(ss + eps)"),
     "rope_sign": ("yi[i] = xi[i] * c - xi[i + half] * s;", "yi[i] = xi[i] * c + xi[i + half] * s;"),
     "rope_pairing": ("double th = (double)pos[t] * inv_freq;", "double th = (double)pos[t] * inv_freq * 2.0;"),
