@@ -15,8 +15,8 @@ The bits of one output row do not depend on batch size, batch neighbours,
 query length, KV-cache length, or eager vs CUDA-graph execution.
 """
 from .api import (add, addmm, bmm, copy4d, debug_wait_probe, embedding, gemm_config,  # noqa: F401
-                  last_device_error, launch_count, linear, matmul, rmsnorm, rope, sdpa, swiglu,
-                  version)
+                  last_device_error, launch_count, linear, matmul, qlinear, rmsnorm, rope, sdpa,
+                  swiglu, version)
 from ._lib import BiError  # noqa: F401
 from .mode import batch_invariant_mode  # noqa: F401
 

@@ -26,6 +26,8 @@ SIGNATURES = {
     "bi_matmul": (_st, [_vp, _i64, _vp, _i64, _vp, _i64, _i64, _i64, _i64, _int, _vp]),
     "bi_matmul_batched": (_st, [_vp, _i64, _i64, _vp, _i64, _i64, _int, _vp, _i64, _i64, _i64,
                                 _i64, _i64, _i64, _int, _vp]),
+    "bi_qlinear": (_st, [_vp, _i64, _vp, _i64, _vp, _vp, _i64, _vp, _vp, _i64, _i64, _i64, _i64,
+                         _int, _int, _int, _vp]),
     "bi_addmm": (_st, [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _i64, _i64, _i64, _f, _f,
                        _int, _vp]),
     "bi_gemm_config": (_st, [_i64, _i64, _int, _int, ctypes.POINTER(_int),

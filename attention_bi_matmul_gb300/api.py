@@ -216,6 +216,38 @@ def matmul(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None) ->
     return y.view(*lead, N) if out is None and y.is_contiguous() else (y if out is None else out)
 
 
+def qlinear(x: torch.Tensor, wq: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor,
+            bits: int, group_size: int, bias: torch.Tensor | None = None,
+            out: torch.Tensor | None = None) -> torch.Tensor:
+    """y = x . w^T (+ bias) with group-wise affine quantized w[N, K]:
+    w[n,k] = scales[n, k//group_size] * q[n,k] + biases[n, k//group_size], q packed in
+    wq (int32 or uint32 [N, K*bits/32]) lowest field first.  Leading dims of x are batch."""
+    dev = _cuda(x, wq, scales, biases, bias, out)
+    lead = x.shape[:-1]
+    x2 = _rows(x, "x")
+    M, K = x2.shape
+    if wq.dim() != 2 or wq.stride(-1) != 1 or wq.element_size() != 4:
+        raise ValueError("qlinear: wq must be a 32-bit [N, K*bits/32] tensor, last dim contiguous")
+    N = wq.shape[0]
+    if scales.shape != biases.shape or scales.dim() != 2 or scales.shape[0] != N:
+        raise ValueError("qlinear: scales/biases must be [N, K/group_size]")
+    if scales.stride(-1) != 1 or biases.stride(-1) != 1 or scales.stride(0) != biases.stride(0):
+        raise ValueError("qlinear: scales and biases need the same contiguous row layout")
+    if scales.dtype != x.dtype or biases.dtype != x.dtype or (
+            bias is not None and (bias.dtype != x.dtype or bias.shape != (N,)
+                                  or not bias.is_contiguous())):
+        raise ValueError("qlinear: dtype/shape mismatch")
+    y = torch.empty((M, N), dtype=x.dtype, device=x.device) if out is None else _rows(out, "out")
+    if y.shape != (M, N):
+        raise ValueError("out must hold [M, N]")
+    with _On(dev) as s:
+        L.check(L.load().bi_qlinear(_p(x2), _ld(x2, K), _p(wq), max(wq.stride(0), wq.shape[1]),
+                                    _p(scales), _p(biases), scales.stride(0) if N > 1 else
+                                    scales.shape[1], _p(bias), _p(y), y.stride(0) if M > 1 else N,
+                                    M, N, K, int(bits), int(group_size), _dt(x), s), "bi_qlinear")
+    return y.view(*lead, N) if out is None else out
+
+
 def addmm(c: torch.Tensor, a: torch.Tensor, b: torch.Tensor, alpha: float = 1.0,
           beta: float = 1.0, out: torch.Tensor | None = None) -> torch.Tensor:
     """y = beta * c + alpha * (a . b); c is [M, N] or a row [N] (broadcast)."""

@@ -119,6 +119,7 @@ bi_status device_init(int dev) {
     if ((st = init_gemm_tc_bf16()) != BI_OK) return st;
     if ((st = init_gemm_tc_f16()) != BI_OK) return st;
     if ((st = init_sdpa()) != BI_OK) return st;
+    if ((st = init_qgemm()) != BI_OK) return st;
     if (!device_error_word()) return BI_ERR_CUDA;
     device_sm_count();
     if (!load_encode()) return BI_ERR_CUDA;
@@ -173,6 +174,25 @@ bi_status encode_tmap(CUtensorMap *map, bi_dtype dt, int rank, void *base, const
                                 CU_TENSOR_MAP_INTERLEAVE_NONE,
                                 swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? BI_OK : BI_ERR_INVALID_ARG;
+}
+
+// Packed 32-bit words (quantized weights), no swizzle: box rows land back to back.
+bi_status encode_tmap_u32(CUtensorMap *map, int rank, void *base, const uint64_t *dims,
+                          const uint64_t *strides_bytes, const uint32_t *box) {
+    if (!load_encode()) return BI_ERR_CUDA;
+    cuuint64_t gdim[5], gstr[4];
+    cuuint32_t bdim[5], estr[5];
+    for (int i = 0; i < rank; ++i) {
+        gdim[i] = dims[i];
+        bdim[i] = box[i];
+        estr[i] = 1;
+    }
+    for (int i = 0; i + 1 < rank; ++i) gstr[i] = strides_bytes[i];
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, static_cast<cuuint32_t>(rank),
+                                base, gdim, gstr, bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? BI_OK : BI_ERR_INVALID_ARG;
 }
@@ -277,6 +297,39 @@ bi_status bi_matmul_batched(const void *a, int64_t lda, int64_t sa, const void *
     args.batch = batch; args.sa = sa; args.sb = sb; args.sy = sy;
     args.epi = EPI_NONE;
     return run_gemm(a, lda, b, ldb, b_nk, args, dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+bi_status bi_qlinear(const void *x, int64_t ldx, const uint32_t *wq, int64_t ldq,
+                     const void *scales, const void *biases, int64_t ldsb, const void *bias,
+                     void *y, int64_t ldy, int64_t M, int64_t N, int64_t K, int bits,
+                     int group_size, bi_dtype dtype, bi_stream_t stream) {
+    if (dtype != BI_BF16 && dtype != BI_F16) return BI_ERR_UNSUPPORTED;
+    if (bits != 2 && bits != 4 && bits != 8) return BI_ERR_UNSUPPORTED;
+    if (group_size != 32 && group_size != 64 && group_size != 128) return BI_ERR_UNSUPPORTED;
+    if (!x || !wq || !scales || !biases || !y) return BI_ERR_INVALID_ARG;
+    if (M < 0 || N <= 0 || K <= 0) return BI_ERR_INVALID_ARG;
+    if (K % group_size) return BI_ERR_INVALID_ARG;
+    if (K % 64) return BI_ERR_UNSUPPORTED;                  // whole 64-wide panels
+    if (ldx < K || ldy < N || ldq < K / 32 * bits || ldsb < K / group_size)
+        return BI_ERR_INVALID_ARG;
+    if (M > (int64_t(1) << 31) || N > (int64_t(1) << 31) || K > (int64_t(1) << 31))
+        return BI_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(wq) || ldx % 8 || ldq % 4) return BI_ERR_ALIGNMENT;
+    if ((reinterpret_cast<uintptr_t>(scales) | reinterpret_cast<uintptr_t>(biases) |
+         reinterpret_cast<uintptr_t>(bias) | reinterpret_cast<uintptr_t>(y)) & 1u)
+        return BI_ERR_ALIGNMENT;
+    if (M == 0) return BI_OK;
+    bi_status st = check_device();
+    if (st != BI_OK) return st;
+    QGemmArgs a{};
+    a.M = M; a.N = N; a.K = K;
+    a.scales = scales; a.biases = biases; a.ldsb = ldsb; a.group_size = group_size;
+    a.bias = bias; a.y = y; a.ldy = ldy;
+    a.err = device_error_word();
+    if (!a.err) return BI_ERR_CUDA;
+    // Token rows each x copy moves; the MMA always spans 64 token columns.
+    a.x_rows = static_cast<int>(M >= 64 ? 64 : ((M + 15) / 16) * 16);
+    return launch_qgemm(x, ldx, wq, ldq, bits, a, dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 
 bi_status bi_addmm(const void *c, int64_t ldc, const void *a, int64_t lda, const void *b,

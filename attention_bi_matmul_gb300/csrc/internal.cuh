@@ -44,6 +44,8 @@ void count_launch();                             // launch counter
 bi_status encode_tmap(CUtensorMap *map, bi_dtype dt, int rank, void *base,
                       const uint64_t *dims, const uint64_t *strides_bytes,
                       const uint32_t *box, bool swizzle128);
+bi_status encode_tmap_u32(CUtensorMap *map, int rank, void *base, const uint64_t *dims,
+                          const uint64_t *strides_bytes, const uint32_t *box);
 TcConfig tc_config(int64_t N, int64_t K, bi_dtype dt, bool b_mn_major);
 bi_status cuda_status(cudaError_t e);
 
@@ -51,12 +53,29 @@ bi_status cuda_status(cudaError_t e);
 bi_status init_gemm_tc_bf16();
 bi_status init_gemm_tc_f16();
 bi_status init_sdpa();
+bi_status init_qgemm();
 
 // ---- launchers
 bi_status launch_gemm_f32(const float *a, int64_t lda, const float *b, int64_t ldb, bool b_nk,
                           const GemmArgs &args, cudaStream_t s);
 bi_status launch_gemm_tc(const void *a, int64_t lda, const void *b, int64_t ldb, bool b_nk,
                          const GemmArgs &args, bi_dtype dt, const TcConfig &cfg, cudaStream_t s);
+
+// Group-wise affine quantized linear: y[M,N] = x[M,K] . w^T (+ bias), with
+// w[n,k] = rnd(scales[n,g] * q[n,k] + biases[n,g]), g = k / group_size.
+struct QGemmArgs {
+    int64_t M, N, K;
+    const void *scales, *biases;  // [N, ldsb] in the activation dtype
+    int64_t ldsb;
+    int group_size;               // 32, 64 or 128
+    const void *bias;             // [N] or null
+    void *y;
+    int64_t ldy;
+    uint32_t *err;
+    int x_rows;                   // token rows each x copy moves: min(64, M rounded up to 16)
+};
+bi_status launch_qgemm(const void *x, int64_t ldx, const uint32_t *wq, int64_t ldq, int bits,
+                       const QGemmArgs &args, bi_dtype dt, cudaStream_t s);
 
 struct SdpaArgs {
     int64_t B, H, Hkv, Lq, Lkv, q_offset;

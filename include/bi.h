@@ -115,6 +115,28 @@ bi_status bi_matmul_batched(const void *a, int64_t lda, int64_t sa, const void *
                             int64_t batch, int64_t M, int64_t N, int64_t K, bi_dtype dtype,
                             bi_stream_t stream);
 
+/* Quantized linear (group-wise affine weights):  y[M,N] = x[M,K] . w^T (+ bias[N])
+ * "mlx-batch-invariant" README, "Quantized models": 2, 4 and 8-bit affine weights,
+ * unpacked inside the K loop of one invariant kernel.  Weight format (the plain
+ * affine reading):
+ *   q[n,k] = field (k mod 32/bits) of word wq[n*ldq + k/(32/bits)], fields of
+ *            `bits` bits counted from the least significant bit;
+ *   w[n,k] = round(scales[n*ldsb + g] * q[n,k] + biases[n*ldsb + g]), g = k/group_size,
+ *            formed with one rounding to the activation dtype.
+ *   x       device [M,K] bf16/fp16, leading dimension ldx >= K (multiple of 8)
+ *   wq      device uint32 [N, ldq], ldq >= K*bits/32 (multiple of 4), 16-byte aligned
+ *   scales, biases  device [N, ldsb] in x's dtype, ldsb >= K/group_size
+ *   bias    device [N] or NULL; added to the fp32 accumulator, rounded once
+ *   y       device [M,N], leading dimension ldy >= N
+ *   bits in {2, 4, 8}; group_size in {32, 64, 128}; K a multiple of 64 and of
+ *   group_size (else BI_ERR_UNSUPPORTED / BI_ERR_INVALID_ARG).
+ * Each output is one fp32 reduction over K in ascending 64-wide panels for
+ * every M: a row's bits do not depend on the number of rows or on the others. */
+bi_status bi_qlinear(const void *x, int64_t ldx, const uint32_t *wq, int64_t ldq,
+                     const void *scales, const void *biases, int64_t ldsb, const void *bias,
+                     void *y, int64_t ldy, int64_t M, int64_t N, int64_t K, int bits,
+                     int group_size, bi_dtype dtype, bi_stream_t stream);
+
 /* Reports the tile configuration the GEMM entry points use for (N, K, dtype,
  * weight layout).  b_layout: 0 = linear (w[N,K]), 1 = matmul/addmm (b[K,N]).
  * Outputs (each may be NULL): block_n = output columns per tile, stages =

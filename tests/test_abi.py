@@ -93,6 +93,27 @@ def test_matmul_batched_validation(lib):
     assert call(sa=12, dt=L.BI_F32) != L.BI_ERR_ALIGNMENT      # fp32 takes any stride
 
 
+def test_qlinear_validation(lib):
+    p = ctypes.c_void_p(4096)
+    s = ctypes.c_void_p(0)
+
+    def call(bits=4, gs=64, K=256, ldq=None, ldx=256, dt=L.BI_BF16, ldsb=None, M=8, xp=p):
+        ldq = K * bits // 32 if ldq is None else ldq
+        ldsb = K // gs if ldsb is None else ldsb
+        return lib.bi_qlinear(xp, ldx, p, ldq, p, p, ldsb, None, p, 64, M, 64, K, bits, gs, dt, s)
+
+    assert call(bits=3) == L.BI_ERR_UNSUPPORTED               # 3-bit packing not built
+    assert call(gs=16) == L.BI_ERR_UNSUPPORTED
+    assert call(dt=L.BI_F32) == L.BI_ERR_UNSUPPORTED
+    assert call(K=96, ldx=96, gs=32) == L.BI_ERR_UNSUPPORTED   # K not a multiple of 64
+    assert call(K=192, ldx=192, gs=128) == L.BI_ERR_INVALID_ARG   # K not a multiple of gs
+    assert call(ldq=16) == L.BI_ERR_INVALID_ARG                # row shorter than K*bits/32
+    assert call(ldsb=3) == L.BI_ERR_INVALID_ARG
+    assert call(ldq=34) == L.BI_ERR_ALIGNMENT                  # 16-byte rows for the copy
+    assert call(xp=ctypes.c_void_p(4104)) == L.BI_ERR_ALIGNMENT
+    assert call(M=0) == L.BI_OK
+
+
 def test_sdpa_validation(lib):
     p = ctypes.c_void_p(4096)
     s = ctypes.c_void_p(0)
