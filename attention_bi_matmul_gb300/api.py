@@ -233,6 +233,15 @@ def qlinear(x: torch.Tensor, wq: torch.Tensor, scales: torch.Tensor, biases: tor
         raise ValueError("qlinear: scales/biases must be [N, K/group_size]")
     if scales.stride(-1) != 1 or biases.stride(-1) != 1 or scales.stride(0) != biases.stride(0):
         raise ValueError("qlinear: scales and biases need the same contiguous row layout")
+    G = scales.shape[1]
+    if scales.stride(0) % 8 or scales.data_ptr() % 16 or biases.data_ptr() % 16:
+        # The library copies scale rows in 16-byte boxes: give it rows padded to a
+        # multiple of 8 elements (a layout copy; pad once ahead of time to avoid it).
+        Gp = (G + 7) // 8 * 8
+        sp = torch.zeros((N, 2, Gp), dtype=scales.dtype, device=scales.device)
+        sp[:, 0, :G] = scales
+        sp[:, 1, :G] = biases
+        scales, biases = sp[:, 0, :G], sp[:, 1, :G]
     if scales.dtype != x.dtype or biases.dtype != x.dtype or (
             bias is not None and (bias.dtype != x.dtype or bias.shape != (N,)
                                   or not bias.is_contiguous())):
@@ -243,7 +252,7 @@ def qlinear(x: torch.Tensor, wq: torch.Tensor, scales: torch.Tensor, biases: tor
     with _On(dev) as s:
         L.check(L.load().bi_qlinear(_p(x2), _ld(x2, K), _p(wq), max(wq.stride(0), wq.shape[1]),
                                     _p(scales), _p(biases), scales.stride(0) if N > 1 else
-                                    scales.shape[1], _p(bias), _p(y), y.stride(0) if M > 1 else N,
+                                    (G + 7) // 8 * 8, _p(bias), _p(y), y.stride(0) if M > 1 else N,
                                     M, N, K, int(bits), int(group_size), _dt(x), s), "bi_qlinear")
     return y.view(*lead, N) if out is None else out
 

@@ -178,9 +178,10 @@ bi_status encode_tmap(CUtensorMap *map, bi_dtype dt, int rank, void *base, const
     return r == CUDA_SUCCESS ? BI_OK : BI_ERR_INVALID_ARG;
 }
 
-// Packed 32-bit words (quantized weights), no swizzle: box rows land back to back.
+// Packed 32-bit words (quantized weights); with swizzle128 the box's 128-byte
+// rows are stored with the 128-byte swizzle (16-byte chunk c of row r at c ^ (r % 8)).
 bi_status encode_tmap_u32(CUtensorMap *map, int rank, void *base, const uint64_t *dims,
-                          const uint64_t *strides_bytes, const uint32_t *box) {
+                          const uint64_t *strides_bytes, const uint32_t *box, bool swizzle128) {
     if (!load_encode()) return BI_ERR_CUDA;
     cuuint64_t gdim[5], gstr[4];
     cuuint32_t bdim[5], estr[5];
@@ -192,7 +193,8 @@ bi_status encode_tmap_u32(CUtensorMap *map, int rank, void *base, const uint64_t
     for (int i = 0; i + 1 < rank; ++i) gstr[i] = strides_bytes[i];
     const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, static_cast<cuuint32_t>(rank),
                                 base, gdim, gstr, bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? BI_OK : BI_ERR_INVALID_ARG;
 }
@@ -315,8 +317,8 @@ bi_status bi_qlinear(const void *x, int64_t ldx, const uint32_t *wq, int64_t ldq
     if (M > (int64_t(1) << 31) || N > (int64_t(1) << 31) || K > (int64_t(1) << 31))
         return BI_ERR_UNSUPPORTED;
     if (!aligned16(x) || !aligned16(wq) || ldx % 8 || ldq % 4) return BI_ERR_ALIGNMENT;
-    if ((reinterpret_cast<uintptr_t>(scales) | reinterpret_cast<uintptr_t>(biases) |
-         reinterpret_cast<uintptr_t>(bias) | reinterpret_cast<uintptr_t>(y)) & 1u)
+    if (!aligned16(scales) || !aligned16(biases) || ldsb % 8) return BI_ERR_ALIGNMENT;
+    if ((reinterpret_cast<uintptr_t>(bias) | reinterpret_cast<uintptr_t>(y)) & 1u)
         return BI_ERR_ALIGNMENT;
     if (M == 0) return BI_OK;
     bi_status st = check_device();

@@ -45,7 +45,7 @@ bi_status encode_tmap(CUtensorMap *map, bi_dtype dt, int rank, void *base,
                       const uint64_t *dims, const uint64_t *strides_bytes,
                       const uint32_t *box, bool swizzle128);
 bi_status encode_tmap_u32(CUtensorMap *map, int rank, void *base, const uint64_t *dims,
-                          const uint64_t *strides_bytes, const uint32_t *box);
+                          const uint64_t *strides_bytes, const uint32_t *box, bool swizzle128);
 TcConfig tc_config(int64_t N, int64_t K, bi_dtype dt, bool b_mn_major);
 bi_status cuda_status(cudaError_t e);
 

@@ -22,18 +22,23 @@
 //   * epilogue: + bias in fp32, one rounding, y[m, n] stored (32 consecutive n
 //     per warp and token: 64-byte segments).
 //
-// Roles (320 threads, persistent over (n block, token block) tiles):
-//   warp 0 lane 0   TMA producer: per panel the x panel (64 tokens x 64 k,
-//                   128-byte swizzle) and the packed weight panel (128 rows x
-//                   8*bits bytes) into one ring stage; L2 prefetch of the
-//                   weight panels one ring further on
-//   warp 1          TMEM allocation (128 columns: two 64-column accumulators);
-//                   lane 0 issues the MMAs
-//   warps 2..9      dequantisers: warp w owns weight rows 32*(w%4)..+31 and
-//                   half (w-2)/4 of each panel's 64 k; they write the 16-bit
-//                   weight panel in the tensor cores' swizzled K-major layout.
-//                   After a tile's last panel they run its epilogue (the warp's
-//                   TMEM lane quarter, token columns 32*half..+31).
+// Roles (608 threads, persistent over (n block, token block) tiles):
+//   warp 0 lane 0   TMA producer of the packed weights: stages of 128 rows x 128
+//                   bytes (16/bits panels; whole 128-byte lines of each row,
+//                   128-byte swizzle so that the dequantisers read without bank
+//                   conflicts), and of the scales and biases: chunks of 8 groups
+//                   x 128 rows
+//   warp 18 lane 0  TMA producer of the x panels (the rows that exist, packed, so
+//                   a decode step keeps up to 32 panels in flight)
+//   warp 1          TMEM allocation (two 64-column accumulators and a ring of 8
+//                   weight panels); lane 0 issues the MMAs
+//   warps 2..17     dequantisers: warp w owns weight rows 32*(w%4)..+31 (its TMEM
+//                   lane quarter) and k [16 part, 16 part + 16) of each panel,
+//                   part = (w-2)/4; they write the 16-bit weights straight into
+//                   tensor memory, where the MMA takes them as its A operand (no
+//                   shared-memory round trip for the largest operand).  After a
+//                   tile's last panel they run its epilogue (the warp's TMEM lane
+//                   quarter, token columns 16 part..+15).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -48,34 +53,45 @@ namespace {
 constexpr int QG_N = 128;      // weight rows per tile (MMA M)
 constexpr int QG_T = 64;       // tokens per tile (MMA N)
 constexpr int QG_K = 64;       // k per panel
-constexpr int QG_THREADS = 320;
-constexpr int QG_DS = 4;       // dequantised weight panels in flight
-constexpr uint32_t QG_XP = QG_T * QG_K * 2;     // 8 KB x panel
-constexpr uint32_t QG_AP = QG_N * QG_K * 2;     // 16 KB dequantised weight panel
-constexpr uint32_t QG_TMEM_COLS = 2 * QG_T;     // 128
+constexpr int QG_DQ = 16;      // dequantising warps: 4 per TMEM lane quarter
+constexpr int QG_THREADS = (QG_DQ + 3) * 32;   // + weight producer, MMA issuer, x producer
+constexpr int QG_XWARP = QG_DQ + 2;            // the x producer's warp
+constexpr int QG_WS = 6;       // packed weight stages in flight (16 KB each)
+constexpr int QG_SS = 4;       // scale/bias chunks in flight (4 KB each)
+constexpr int QG_XS_MAX = 32;  // x panels in flight: 64 KB / (x_rows * 128 bytes), at most 32
+constexpr int QG_DS = 8;       // dequantised weight panels in flight (tensor memory)
+constexpr uint32_t QG_WSTAGE = QG_N * 128;      // 16 KB: 128 rows x 128 packed bytes
+constexpr uint32_t QG_SCHUNK = QG_N * 16;       // 2 KB: 128 rows x 8 groups x 2 bytes
+constexpr uint32_t QG_XREGION = 64 * 1024;      // x ring
+// Tensor memory: two 64-column fp32 accumulators, then DS dequantised weight
+// panels of 32 columns (64 16-bit weights per row, two per column).
+constexpr uint32_t QG_A_COL = 2 * QG_T;         // first column of the weight panels
+constexpr uint32_t QG_TMEM_COLS = 512;          // 128 + 8 * 32 = 384 used
 
-// Raw ring depth by width: enough packed weight bytes in flight per SM.
-template <int BITS> __host__ __device__ constexpr int qg_rs() {
-    return BITS == 2 ? 10 : BITS == 4 ? 8 : 6;
-}
-template <int BITS> __host__ __device__ constexpr uint32_t qg_wraw() {
-    return QG_N * QG_K * BITS / 8;   // packed bytes of one weight panel
-}
+// Panels per packed stage: 128 bytes of a row hold 1024 / BITS weights.
+template <int BITS> __host__ __device__ constexpr int qg_pps() { return 16 / BITS; }
 
-template <int BITS>
 struct QgSmem {
-    static constexpr uint32_t RS = qg_rs<BITS>();
     // byte offsets from the 1024-aligned base
-    static constexpr uint32_t X = 0;                                // [RS] x panels
-    static constexpr uint32_t A = X + RS * QG_XP;                   // [DS] weight panels
-    static constexpr uint32_t W = A + QG_DS * QG_AP;                // [RS] packed panels
-    static constexpr uint32_t BARS = W + RS * qg_wraw<BITS>();
-    // raw_full[RS] raw_empty[RS] a_full[DS] a_empty[DS] tfull[2] tempty[2] mma_done
-    static constexpr uint32_t NBARS = 2 * RS + 2 * QG_DS + 4 + 1;
+    static constexpr uint32_t W = 0;                                // [WS] packed stages
+    static constexpr uint32_t X = W + QG_WS * QG_WSTAGE;            // x panels, packed
+    static constexpr uint32_t SB = X + QG_XREGION;                  // [SS] scales, biases
+    static constexpr uint32_t BARS = SB + QG_SS * 2 * QG_SCHUNK;
+    // w_full[WS] w_empty[WS] s_full[SS] s_empty[SS] x_full[XS_MAX] x_empty[XS_MAX]
+    // a_full[DS] a_empty[DS] tfull[2] tempty[2] mma_done (the x and a rings are
+    // used per batch of panels: fewer slots than their arrays hold)
+    static constexpr uint32_t NBARS =
+        2 * QG_WS + 2 * QG_SS + 2 * QG_XS_MAX + 2 * QG_DS + 4 + 1;
     static constexpr uint32_t MISC = BARS + NBARS * 8;               // tmem slot, abort flag
     static constexpr uint32_t END = MISC + 16;
     static constexpr size_t BYTES = 1024 + END;
 };
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
 
 // Fields 2j and 2j+1 (bit offsets OA and OA + BITS) of w in the two 16-bit halves.
 template <int BITS, int OA>
@@ -84,13 +100,7 @@ __device__ __forceinline__ uint32_t field_pair(uint32_t w) {
     constexpr int OB = OA + BITS;
     const uint32_t lo = w >> OA;
     const uint32_t hi = OB >= 16 ? (w >> (OB - 16)) : (w << (16 - OB));
-    return (lo & MASK) | (hi & (MASK << 16));
-}
-
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-    uint32_t d;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-    return d;
+    return prmt(lo, hi, 0x7610u) & (MASK | (MASK << 16));   // low half of lo, high half of hi
 }
 
 template <typename T> struct Pair;
@@ -104,18 +114,18 @@ template <typename P> __device__ __forceinline__ uint32_t as_u32(P p) {
     return *reinterpret_cast<uint32_t *>(&p);
 }
 
-// q pair (exact small integers in the 16-bit type) from two fields in 16-bit halves:
-// the field becomes the low mantissa bits of a constant whose unit in the last
-// place is 1 (bf16 128 + q for q < 128, fp16 1024 + q for q < 1024), then the
-// constant is subtracted exactly.
-template <typename T> __device__ __forceinline__ uint32_t q_pair(uint32_t halves);
-template <> __device__ __forceinline__ uint32_t q_pair<__nv_bfloat16>(uint32_t halves) {
-    const __nv_bfloat162 v = as_pair<__nv_bfloat162>(halves | 0x43004300u);   // 128 + q
-    return as_u32(__hsub2(v, as_pair<__nv_bfloat162>(0x43004300u)));
-}
-template <> __device__ __forceinline__ uint32_t q_pair<__half>(uint32_t halves) {
-    const __half2 v = as_pair<__half2>(halves | 0x64006400u);                 // 1024 + q
-    return as_u32(__hsub2(v, as_pair<__half2>(0x64006400u)));
+// The 16-bit pattern whose low byte holds a field and whose value is MAGIC + field,
+// with a unit in the last place of 1: bf16 0x43xx = 128 + q (q < 128), fp16
+// 0x64xx = 1024 + q (q < 256 with a byte field).
+template <typename T> struct Magic;
+template <> struct Magic<__nv_bfloat16> { static constexpr uint32_t byte = 0x43u; };
+template <> struct Magic<__half> { static constexpr uint32_t byte = 0x64u; };
+
+// q pair from a pair whose two halves are (MAGIC + q): one exact subtraction.
+template <typename T> __device__ __forceinline__ uint32_t q_from_magic(uint32_t v) {
+    using P = typename Pair<T>::t;
+    constexpr uint32_t mm = (Magic<T>::byte << 24) | (Magic<T>::byte << 8);
+    return as_u32(__hsub2(as_pair<P>(v), as_pair<P>(mm)));
 }
 
 // rnd(s * q + b) for a pair: one fused multiply-add, one rounding.
@@ -130,18 +140,26 @@ __device__ __forceinline__ uint32_t deq_pair(uint32_t q2, uint32_t s2, uint32_t 
 // of a word (`sub` = 0 / 1).
 template <typename T, int BITS>
 __device__ __forceinline__ uint4 deq8(const uint32_t *w, int sub, uint32_t s2, uint32_t b2) {
+    constexpr uint32_t KM = Magic<T>::byte * 0x01010101u;
     uint32_t q[4];
     if constexpr (BITS == 4) {
-        q[0] = q_pair<T>(field_pair<4, 0>(w[0]));
-        q[1] = q_pair<T>(field_pair<4, 8>(w[0]));
-        q[2] = q_pair<T>(field_pair<4, 16>(w[0]));
-        q[3] = q_pair<T>(field_pair<4, 24>(w[0]));
+        // nibbles n0..n7 of the word -> bytes [n0 n1 n2 n3], [n4 n5 n6 n7] -> pairs
+        // [n, MAGIC, n', MAGIC] (value MAGIC + n in each half)
+        const uint32_t ev = w[0] & 0x0F0F0F0Fu;          // n0 n2 n4 n6
+        const uint32_t od = (w[0] >> 4) & 0x0F0F0F0Fu;   // n1 n3 n5 n7
+        const uint32_t lo = prmt(ev, od, 0x5140u);       // n0 n1 n2 n3
+        const uint32_t hi = prmt(ev, od, 0x7362u);       // n4 n5 n6 n7
+        q[0] = q_from_magic<T>(prmt(lo, KM, 0x5140u));
+        q[1] = q_from_magic<T>(prmt(lo, KM, 0x7362u));
+        q[2] = q_from_magic<T>(prmt(hi, KM, 0x5140u));
+        q[3] = q_from_magic<T>(prmt(hi, KM, 0x7362u));
     } else if constexpr (BITS == 2) {
         const uint32_t v = sub ? (w[0] >> 16) : w[0];
-        q[0] = q_pair<T>(field_pair<2, 0>(v));
-        q[1] = q_pair<T>(field_pair<2, 4>(v));
-        q[2] = q_pair<T>(field_pair<2, 8>(v));
-        q[3] = q_pair<T>(field_pair<2, 12>(v));
+        constexpr uint32_t MM = (Magic<T>::byte << 24) | (Magic<T>::byte << 8);
+        q[0] = q_from_magic<T>(field_pair<2, 0>(v) | MM);
+        q[1] = q_from_magic<T>(field_pair<2, 4>(v) | MM);
+        q[2] = q_from_magic<T>(field_pair<2, 8>(v) | MM);
+        q[3] = q_from_magic<T>(field_pair<2, 12>(v) | MM);
     } else {   // BITS == 8
         if constexpr (IsBf16<T>::value) {
             // q up to 255 needs 8 significant bits: form it exactly in fp32
@@ -155,44 +173,43 @@ __device__ __forceinline__ uint4 deq8(const uint32_t *w, int sub, uint32_t s2, u
                 q[i] = as_u32(__floats2bfloat162_rn(fa, fb));
             }
         } else {
-            // bytes (2i, 2i+1) of the two words straight into the fp16 halves
-            q[0] = q_pair<T>(prmt(w[0], 0u, 0x7170u) & 0x00FF00FFu);
-            q[1] = q_pair<T>(prmt(w[0], 0u, 0x7372u) & 0x00FF00FFu);
-            q[2] = q_pair<T>(prmt(w[1], 0u, 0x7170u) & 0x00FF00FFu);
-            q[3] = q_pair<T>(prmt(w[1], 0u, 0x7372u) & 0x00FF00FFu);
+            // bytes straight into the halves next to the magic byte: 1024 + q
+            q[0] = q_from_magic<T>(prmt(w[0], KM, 0x4140u));
+            q[1] = q_from_magic<T>(prmt(w[0], KM, 0x4342u));
+            q[2] = q_from_magic<T>(prmt(w[1], KM, 0x4140u));
+            q[3] = q_from_magic<T>(prmt(w[1], KM, 0x4342u));
         }
     }
     return make_uint4(deq_pair<T>(q[0], s2, b2), deq_pair<T>(q[1], s2, b2),
                       deq_pair<T>(q[2], s2, b2), deq_pair<T>(q[3], s2, b2));
 }
 
-__device__ __forceinline__ uint32_t ld_u16_nc(const void *p) {
-    unsigned short v;
-    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
-    return v;
-}
-
 template <typename T, int BITS>
 __global__ void __launch_bounds__(QG_THREADS, 1)
     qgemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                 const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmB,
                  const QGemmArgs args) {
-    using S = QgSmem<BITS>;
-    constexpr int RS = S::RS;
-    constexpr uint32_t WRAW = qg_wraw<BITS>();
-    constexpr uint32_t WROW = QG_K * BITS / 8;          // packed bytes of one row's panel
-    constexpr int WPP = QG_K * BITS / 32;               // packed words of one row's panel
+    using S = QgSmem;
+    constexpr int PPS = qg_pps<BITS>();                 // panels per packed stage
+    constexpr int KPT = QG_K / (QG_DQ / 4);             // k of a panel row per thread (16)
+    constexpr uint32_t QB = KPT * BITS / 8;             // their packed bytes
+    constexpr int QB_B = PPS < 4 ? PPS : 4;             // panels per dequantising batch
     constexpr uint32_t IDESC = mma_idesc(IsBf16<T>::value, QG_N, QG_T, false);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
-    uint8_t *sX = smem + S::X;
-    uint8_t *sA = smem + S::A;
     uint8_t *sW = smem + S::W;
+    uint8_t *sX = smem + S::X;
+    uint8_t *sSB = smem + S::SB;     // chunk c: scales at c * 4 KB, biases 2 KB further
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::BARS);
-    uint64_t *raw_full = bars;
-    uint64_t *raw_empty = raw_full + RS;
-    uint64_t *a_full = raw_empty + RS;
+    uint64_t *w_full = bars;
+    uint64_t *w_empty = w_full + QG_WS;
+    uint64_t *s_full = w_empty + QG_WS;
+    uint64_t *s_empty = s_full + QG_SS;
+    uint64_t *x_full = s_empty + QG_SS;
+    uint64_t *x_empty = x_full + QG_XS_MAX;
+    uint64_t *a_full = x_empty + QG_XS_MAX;
     uint64_t *a_empty = a_full + QG_DS;
     uint64_t *tfull = a_empty + QG_DS;
     uint64_t *tempty = tfull + 2;
@@ -208,19 +225,43 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
     const int64_t num_t = (M + QG_T - 1) / QG_T;
     const int64_t total = num_n * num_t;
     const int KP = static_cast<int>(K / QG_K);          // panels per tile (K % 64 == 0)
+    const int KW = (KP + PPS - 1) / PPS;                // packed stages per tile
+    const int gs = args.group_size;
+    const int lg = gs == 32 ? 5 : gs == 64 ? 6 : 7;     // log2(group size)
+    const int PPC = gs / 8;                             // panels per scale chunk (8 groups)
+    const int NC = static_cast<int>((K / gs + 7) / 8);  // scale chunks per tile
+    // x panels are packed at x_rows * 128 bytes (a multiple of 2 KB, so every panel
+    // starts on the 1024-byte swizzle period).  The MMA reads 64 token rows; rows
+    // past x_rows hold whatever follows and only feed output columns that are
+    // never stored.
+    const uint32_t XB = static_cast<uint32_t>(args.x_rows) * 128;
+    // The x ring and the tensor-memory weight ring go by batches of QB_B panels (one
+    // barrier, one copy and one commit per batch): XS batch slots of QB_B x panels,
+    // DSB batch slots of QB_B weight panels.
+    const uint32_t XBB = XB * QB_B;                     // bytes of a batch of x panels
+    const int XS = static_cast<int>(QG_XREGION / XBB < QG_XS_MAX ? QG_XREGION / XBB : QG_XS_MAX);
+    constexpr int DSB = QG_DS / QB_B;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < RS; ++s) {
-            mbar_init(&raw_full[s], 1);
-            mbar_init(&raw_empty[s], 1 + 8);   // the MMA's commit (x) + 8 dequantisers (w)
+        for (int i = 0; i < QG_WS; ++i) {
+            mbar_init(&w_full[i], 1);
+            mbar_init(&w_empty[i], QG_DQ);  // the dequantisers
         }
-        for (int d = 0; d < QG_DS; ++d) {
-            mbar_init(&a_full[d], 8);
-            mbar_init(&a_empty[d], 1);
+        for (int i = 0; i < QG_SS; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_empty[i], QG_DQ);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], 8);
+        for (int i = 0; i < QG_XS_MAX; ++i) {
+            mbar_init(&x_full[i], 1);
+            mbar_init(&x_empty[i], 1);      // the MMA's commit
+        }
+        for (int i = 0; i < QG_DS; ++i) {
+            mbar_init(&a_full[i], QG_DQ);
+            mbar_init(&a_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&tfull[i], 1);
+            mbar_init(&tempty[i], QG_DQ);
         }
         mbar_init(mma_done, 1);
         *abort_flag = 0;
@@ -237,60 +278,102 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            // ------------------------------------------------ TMA producer
-            prefetch_tmap(&tmX);
+            // ------------------------------------------------ TMA producer: weights, scales
             prefetch_tmap(&tmW);
-            const uint32_t tx = static_cast<uint32_t>(args.x_rows) * QG_K * 2 + WRAW;
-            uint32_t it = 0, s = 0, ph = 0;
+            prefetch_tmap(&tmS);
+            prefetch_tmap(&tmB);
+            uint32_t nw = 0, ns = 0, ws = 0, wph = 0, ss = 0, sph = 0;
             bool ok = true;
             for (int64_t t = blockIdx.x; ok && t < total; t += gridDim.x) {
-                const int64_t nb = t % num_n, tb = t / num_n;
-                const int32_t wrow = static_cast<int32_t>(nb * QG_N);
-                for (int p = 0; p < RS && p < KP; ++p)
-                    tma_prefetch_2d(&tmW, p * WPP, wrow);
-                for (int p = 0; p < KP; ++p, ++it) {
-                    if (!mbar_wait(&raw_empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&raw_full[s], tx);
-                    tma_load_2d(sX + s * QG_XP, &tmX, &raw_full[s], p * QG_K,
-                                static_cast<int32_t>(tb * QG_T));
-                    tma_load_2d(sW + s * WRAW, &tmW, &raw_full[s], p * WPP, wrow);
-                    if (p + RS < KP) tma_prefetch_2d(&tmW, (p + RS) * WPP, wrow);
-                    if (++s == RS) { s = 0; ph ^= 1u; }
+                const int32_t wrow = static_cast<int32_t>((t % num_n) * QG_N);
+                int c = 0;
+                for (int st = 0; ok && st < KW; ++st) {
+                    if (!mbar_wait(&w_empty[ws], wph ^ 1u, abort_flag)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&w_full[ws], QG_WSTAGE);
+                    tma_load_2d(sW + ws * QG_WSTAGE, &tmW, &w_full[ws], st * 32, wrow);
+                    ++nw;
+                    if (++ws == QG_WS) { ws = 0; wph ^= 1u; }
+                    // the scale chunks whose first panel lies in this stage
+                    for (; c < NC && c * PPC < (st + 1) * PPS; ++c) {
+                        if (!mbar_wait(&s_empty[ss], sph ^ 1u, abort_flag)) { ok = false; break; }
+                        mbar_arrive_expect_tx(&s_full[ss], 2 * QG_SCHUNK);
+                        uint8_t *dst = sSB + ss * 2 * QG_SCHUNK;
+                        tma_load_2d(dst, &tmS, &s_full[ss], c * 8, wrow);
+                        tma_load_2d(dst + QG_SCHUNK, &tmB, &s_full[ss], c * 8, wrow);
+                        ++ns;
+                        if (++ss == QG_SS) { ss = 0; sph ^= 1u; }
+                    }
                 }
             }
             if (!ok) {
                 // Let every copy already issued land before the block can exit.
-                const uint32_t first = it > static_cast<uint32_t>(RS) ? it - RS : 0;
-                for (uint32_t i = first; i < it; ++i)
-                    mbar_wait_limited(&raw_full[i % RS], (i / RS) & 1u, WAIT_LIMIT_NS);
+                for (uint32_t i = nw > QG_WS ? nw - QG_WS : 0; i < nw; ++i)
+                    mbar_wait_limited(&w_full[i % QG_WS], (i / QG_WS) & 1u, WAIT_LIMIT_NS);
+                for (uint32_t i = ns > QG_SS ? ns - QG_SS : 0; i < ns; ++i)
+                    mbar_wait_limited(&s_full[i % QG_SS], (i / QG_SS) & 1u, WAIT_LIMIT_NS);
+            }
+        }
+    } else if (warp == QG_XWARP) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer: x panels
+            prefetch_tmap(&tmX);
+            uint32_t nx = 0;
+            int xs = 0;
+            uint32_t xph = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; ok && t < total; t += gridDim.x) {
+                const int32_t trow = static_cast<int32_t>((t / num_n) * QG_T);
+                for (int p0 = 0; p0 < KP; p0 += QB_B) {
+                    const int nb_ = KP - p0 < QB_B ? KP - p0 : QB_B;
+                    if (!mbar_wait(&x_empty[xs], xph ^ 1u, abort_flag)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&x_full[xs], XB * nb_);
+                    for (int b = 0; b < nb_; ++b)
+                        tma_load_2d(sX + xs * XBB + b * XB, &tmX, &x_full[xs], (p0 + b) * QG_K, trow);
+                    ++nx;
+                    if (++xs == XS) { xs = 0; xph ^= 1u; }
+                }
+            }
+            if (!ok) {
+                for (uint32_t i = nx > static_cast<uint32_t>(XS) ? nx - XS : 0; i < nx; ++i)
+                    mbar_wait_limited(&x_full[i % XS], (i / XS) & 1u, WAIT_LIMIT_NS);
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------------ MMA issuer
-            const uint64_t a_desc0 = smem_desc(smem_u32(sA), 16, 1024);
             const uint64_t x_desc0 = smem_desc(smem_u32(sX), 16, 1024);
-            uint32_t tc = 0, s = 0, ph = 0, d = 0, dph = 0;
+            uint32_t tc = 0, xph = 0, d = 0, dph = 0;
+            int xs = 0;
             bool ok = true;
             for (int64_t t = blockIdx.x; ok && t < total; t += gridDim.x, ++tc) {
                 const uint32_t acc = tc & 1u;
                 if (!mbar_wait(&tempty[acc], ((tc >> 1) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * QG_T;
-                for (int p = 0; p < KP; ++p) {
+                // Batches of QB_B panels, as the dequantisers hand them over: every
+                // warp arrives on a batch's panels in order, so the last panel's
+                // barrier completing means the batch is in tensor memory.
+                for (int p0 = 0; ok && p0 < KP; p0 += QB_B) {
+                    const int nb_ = KP - p0 < QB_B ? KP - p0 : QB_B;
                     if (!mbar_wait(&a_full[d], dph, abort_flag)) { ok = false; break; }
-                    if (!mbar_wait(&raw_full[s], ph, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(&x_full[xs], xph, abort_flag)) { ok = false; break; }
                     tc_fence_after();
-                    const uint64_t ad = a_desc0 + ((d * QG_AP) >> 4);
-                    const uint64_t xd = x_desc0 + ((s * QG_XP) >> 4);
+                    const uint32_t a_tmem = tmem_base + QG_A_COL + d * QB_B * (QG_K / 2);
+                    const uint64_t xd = x_desc0 + ((xs * XBB) >> 4);
 #pragma unroll
-                    for (int j = 0; j < QG_K / 16; ++j)
-                        mma_f16_ss(d_tmem, ad + j * (32 >> 4), xd + j * (32 >> 4), IDESC,
-                                   (p | j) != 0 ? 1u : 0u);
+                    for (int b = 0; b < QB_B; ++b) {
+                        if (b < nb_) {
+#pragma unroll
+                            for (int j = 0; j < QG_K / 16; ++j)   // 16 k = 8 columns of A
+                                mma_f16_ts(d_tmem, a_tmem + b * (QG_K / 2) + j * 8,
+                                           xd + ((b * XB) >> 4) + j * (32 >> 4), IDESC,
+                                           (p0 + b + j) != 0 ? 1u : 0u);
+                        }
+                    }
                     mma_commit(&a_empty[d]);
-                    mma_commit(&raw_empty[s]);
-                    if (++d == QG_DS) { d = 0; dph ^= 1u; }
-                    if (++s == RS) { s = 0; ph ^= 1u; }
+                    mma_commit(&x_empty[xs]);
+                    if (++d == DSB) { d = 0; dph ^= 1u; }
+                    if (++xs == XS) { xs = 0; xph ^= 1u; }
                 }
                 if (!ok) break;
                 mma_commit(&tfull[acc]);
@@ -299,83 +382,107 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
             mma_commit(mma_done);
             mbar_wait_limited(mma_done, 0, WAIT_LIMIT_NS);
         }
-    } else {
-        // ------------------------------------------------ dequantisers + epilogue (2..9)
-        using Tv = T;
+    } else if (warp >= 2 && warp < 2 + QG_DQ) {
+        // ------------------------------------------------ dequantisers + epilogue
         const uint32_t quarter = static_cast<uint32_t>(warp & 3);
-        const int half = (warp - 2) >> 2;
+        const int part = (warp - 2) >> 2;                        // k [KPT part, +KPT) of a panel
         const int r = static_cast<int>(quarter) * 32 + lane;     // weight row in the tile
-        const int gs = args.group_size;
-        const Tv *scales = static_cast<const Tv *>(args.scales);
-        const Tv *biases = static_cast<const Tv *>(args.biases);
-        uint32_t tc = 0, s = 0, ph = 0, d = 0, dph = 0;
+        uint32_t tc = 0, ws = 0, wph = 0, ss = 0, sph = 0, d = 0, dph = 0;
         bool ok = true;
         for (int64_t t = blockIdx.x; ok && t < total; t += gridDim.x, ++tc) {
             const int64_t nb = t % num_n, tb = t / num_n;
             const int64_t n = nb * QG_N + r;
-            const bool nvalid = n < N;
-            const int64_t sb_row = (nvalid ? n : 0) * args.ldsb;
-            for (int p = 0; p < KP; ++p) {
-                // this thread's group: k0 = 64 p + 32 half lies in one group (gs >= 32)
-                const int64_t g = (static_cast<int64_t>(p) * QG_K + half * 32) / gs;
-                uint32_t sv = 0, bv = 0;
-                if (nvalid) {
-                    sv = ld_u16_nc(scales + sb_row + g);
-                    bv = ld_u16_nc(biases + sb_row + g);
+            // Panels go in batches of QB_B: one wait per packed stage and per scale chunk
+            // (a batch never straddles either: QB_B divides both), the batch's math is
+            // independent work, and one TMEM store completion covers the batch.
+            for (int p0 = 0; ok && p0 < KP; p0 += QB_B) {
+                const int il0 = p0 % PPS;                   // first panel within its stage
+                if (il0 == 0 && !warp_wait(&w_full[ws], wph, abort_flag)) { ok = false; break; }
+                if ((p0 & (PPC - 1)) == 0 && !warp_wait(&s_full[ss], sph, abort_flag)) {
+                    ok = false;
+                    break;
                 }
-                const uint32_t s2 = sv | (sv << 16), b2 = bv | (bv << 16);
-                if (!warp_wait(&raw_full[s], ph, abort_flag)) { ok = false; break; }
-                // this row's packed words for k in [32 half, 32 half + 32)
-                uint32_t wv[WPP / 2];
-                const uint8_t *src = sW + s * WRAW + r * WROW + half * (WROW / 2);
-                if constexpr (WPP / 2 == 1) {
-                    wv[0] = *reinterpret_cast<const uint32_t *>(src);
-                } else if constexpr (WPP / 2 == 2) {
-                    const uint2 u = *reinterpret_cast<const uint2 *>(src);
-                    wv[0] = u.x; wv[1] = u.y;
-                } else {
+                const uint8_t *wrow = sW + ws * QG_WSTAGE + r * 128;
+                const uint8_t *sbrow = sSB + ss * 2 * QG_SCHUNK + r * 16;
+                uint32_t out[QB_B][KPT / 2];
 #pragma unroll
-                    for (int i = 0; i < WPP / 2; i += 4) {
-                        const uint4 u = *reinterpret_cast<const uint4 *>(src + 4 * i);
-                        wv[i] = u.x; wv[i + 1] = u.y; wv[i + 2] = u.z; wv[i + 3] = u.w;
+                for (int b = 0; b < QB_B; ++b) {
+                    const int p = p0 + b;
+                    if (p < KP) {
+                        // this thread's group (k0 = 64 p + KPT part lies in one group)
+                        const int j = ((p * QG_K + part * KPT) >> lg) & 7;
+                        const uint32_t sv = *reinterpret_cast<const uint16_t *>(sbrow + j * 2);
+                        const uint32_t bv =
+                            *reinterpret_cast<const uint16_t *>(sbrow + QG_SCHUNK + j * 2);
+                        const uint32_t s2 = sv | (sv << 16), b2 = bv | (bv << 16);
+                        // packed bytes for k in [64 p + KPT part, +KPT): byte offset o of
+                        // the stage row's 128, in 16-byte chunks with the 128-byte swizzle
+                        uint32_t wv[QB / 4];
+                        const uint32_t o = static_cast<uint32_t>((il0 + b) * 8 * BITS) + part * QB;
+                        const uint8_t *src = wrow + (((o >> 4) ^ (r & 7)) << 4) + (o & 15);
+                        if constexpr (QB == 16) {
+                            const uint4 u = *reinterpret_cast<const uint4 *>(src);
+                            wv[0] = u.x; wv[1] = u.y; wv[2] = u.z; wv[3] = u.w;
+                        } else if constexpr (QB == 8) {
+                            const uint2 u = *reinterpret_cast<const uint2 *>(src);
+                            wv[0] = u.x; wv[1] = u.y;
+                        } else {
+                            wv[0] = *reinterpret_cast<const uint32_t *>(src);
+                        }
+#pragma unroll
+                        for (int c = 0; c < KPT / 8; ++c) {
+                            uint4 v;
+                            if constexpr (BITS == 4) v = deq8<T, 4>(&wv[c], 0, s2, b2);
+                            else if constexpr (BITS == 8) v = deq8<T, 8>(&wv[2 * c], 0, s2, b2);
+                            else v = deq8<T, 2>(&wv[0], c, s2, b2);
+                            out[b][4 * c] = v.x; out[b][4 * c + 1] = v.y;
+                            out[b][4 * c + 2] = v.z; out[b][4 * c + 3] = v.w;
+                        }
                     }
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&raw_empty[s]);
-                if (!warp_wait(&a_empty[d], dph ^ 1u, abort_flag)) { ok = false; break; }
-                uint8_t *dst = sA + d * QG_AP + r * 128;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int chunk = half * 4 + c;                    // 8 weights each
-                    uint4 v;
-                    if constexpr (BITS == 4) v = deq8<T, 4>(&wv[c], 0, s2, b2);
-                    else if constexpr (BITS == 8) v = deq8<T, 8>(&wv[2 * c], 0, s2, b2);
-                    else v = deq8<T, 2>(&wv[c >> 1], c & 1, s2, b2);
-                    *reinterpret_cast<uint4 *>(dst + ((chunk ^ (r & 7)) << 4)) = v;
+                // release the scale chunk / packed stage when this batch ends it
+                const int pl = (p0 + QB_B < KP ? p0 + QB_B : KP) - 1;   // last panel of the batch
+                if ((pl & (PPC - 1)) == PPC - 1 || pl == KP - 1) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&s_empty[ss]);
+                    if (++ss == QG_SS) { ss = 0; sph ^= 1u; }
                 }
-                fence_proxy_async_smem();
+                if (pl % PPS == PPS - 1 || pl == KP - 1) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&w_empty[ws]);
+                    if (++ws == QG_WS) { ws = 0; wph ^= 1u; }
+                }
+                // KPT weights = KPT/2 columns of this row's TMEM lane in each panel of
+                // batch slot d
+                if (!warp_wait(&a_empty[d], dph ^ 1u, abort_flag)) { ok = false; break; }
+                const uint32_t a_col = tmem_base + ((quarter * 32u) << 16) + QG_A_COL +
+                                       d * QB_B * (QG_K / 2) + part * (KPT / 2);
+#pragma unroll
+                for (int b = 0; b < QB_B; ++b)
+                    if (p0 + b < KP) tmem_st8(a_col + b * (QG_K / 2), out[b]);
+                tmem_wait_st();
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&a_full[d]);
-                if (++d == QG_DS) { d = 0; dph ^= 1u; }
-                if (++s == RS) { s = 0; ph ^= 1u; }
+                if (++d == DSB) { d = 0; dph ^= 1u; }
             }
             if (!ok) break;
-            // ---------------- epilogue of this tile: rows r, token columns 32 half..+31
+            // ---------------- epilogue of this tile: rows r, token columns 16 part..+15
             const uint32_t acc = tc & 1u;
             if (!warp_wait(&tfull[acc], (tc >> 1) & 1u, abort_flag)) break;
             tc_fence_after();
-            uint32_t v[32];
-            tmem_ld32(tmem_base + ((quarter * 32u) << 16) + acc * QG_T + half * 32, v);
-            tmem_wait_ld(v);
+            uint32_t v[16];
+            tmem_ld16(tmem_base + ((quarter * 32u) << 16) + acc * QG_T + part * 16, v);
+            tmem_wait_ld16(v);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[acc]);
-            if (nvalid) {
+            if (n < N) {
                 const float bn = args.bias ? to_f32<T>(static_cast<const T *>(args.bias)[n]) : 0.0f;
                 T *ycol = static_cast<T *>(args.y) + n;
-                const int64_t m0 = tb * QG_T + half * 32;
+                const int64_t m0 = tb * QG_T + part * 16;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
+                for (int i = 0; i < 16; ++i) {
                     const int64_t m = m0 + i;
                     if (m < M) {
                         float a = __uint_as_float(v[i]);
@@ -399,27 +506,28 @@ template <typename T, int BITS>
 bi_status qgemm_attr() {
     return cuda_status(cudaFuncSetAttribute(qgemm_kernel<T, BITS>,
                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            static_cast<int>(QgSmem<BITS>::BYTES)));
+                                            static_cast<int>(QgSmem::BYTES)));
 }
 
 template <typename T, int BITS>
-bi_status qgemm_launch(const CUtensorMap &tx, const CUtensorMap &tw, const QGemmArgs &args,
-                       cudaStream_t s) {
+bi_status qgemm_launch(const CUtensorMap &tx, const CUtensorMap &tw, const CUtensorMap &ts,
+                       const CUtensorMap &tb, const QGemmArgs &args, cudaStream_t s) {
     const int64_t tiles = ((args.N + QG_N - 1) / QG_N) * ((args.M + QG_T - 1) / QG_T);
     const int sms = device_sm_count();
     const int grid = static_cast<int>(tiles < sms ? tiles : sms);
-    qgemm_kernel<T, BITS><<<grid, QG_THREADS, QgSmem<BITS>::BYTES, s>>>(tx, tw, args);
+    qgemm_kernel<T, BITS><<<grid, QG_THREADS, QgSmem::BYTES, s>>>(tx, tw, ts, tb, args);
     count_launch();
     return cuda_status(cudaGetLastError());
 }
 
 template <typename T>
 bi_status qgemm_bits(int bits, const CUtensorMap &tx, const CUtensorMap &tw,
-                     const QGemmArgs &args, cudaStream_t s) {
+                     const CUtensorMap &ts, const CUtensorMap &tb, const QGemmArgs &args,
+                     cudaStream_t s) {
     switch (bits) {
-        case 2: return qgemm_launch<T, 2>(tx, tw, args, s);
-        case 4: return qgemm_launch<T, 4>(tx, tw, args, s);
-        case 8: return qgemm_launch<T, 8>(tx, tw, args, s);
+        case 2: return qgemm_launch<T, 2>(tx, tw, ts, tb, args, s);
+        case 4: return qgemm_launch<T, 4>(tx, tw, ts, tb, args, s);
+        case 8: return qgemm_launch<T, 8>(tx, tw, ts, tb, args, s);
         default: return BI_ERR_UNSUPPORTED;
     }
 }
@@ -439,7 +547,7 @@ bi_status init_qgemm() {
 
 bi_status launch_qgemm(const void *x, int64_t ldx, const uint32_t *wq, int64_t ldq, int bits,
                        const QGemmArgs &args, bi_dtype dt, cudaStream_t s) {
-    CUtensorMap tx, tw;
+    CUtensorMap tx, tw, ts, tb;
     {
         const uint64_t dims[2] = {static_cast<uint64_t>(args.K), static_cast<uint64_t>(args.M)};
         const uint64_t strides[1] = {static_cast<uint64_t>(ldx) * 2};
@@ -451,12 +559,25 @@ bi_status launch_qgemm(const void *x, int64_t ldx, const uint32_t *wq, int64_t l
         const uint64_t dims[2] = {static_cast<uint64_t>(args.K * bits / 32),
                                   static_cast<uint64_t>(args.N)};
         const uint64_t strides[1] = {static_cast<uint64_t>(ldq) * 4};
-        const uint32_t box[2] = {static_cast<uint32_t>(QG_K * bits / 32), QG_N};
-        bi_status st = encode_tmap_u32(&tw, 2, const_cast<uint32_t *>(wq), dims, strides, box);
+        const uint32_t box[2] = {32, QG_N};     // 128 packed bytes of 128 rows, 128-byte swizzle
+        bi_status st =
+            encode_tmap_u32(&tw, 2, const_cast<uint32_t *>(wq), dims, strides, box, true);
         if (st != BI_OK) return st;
     }
-    if (dt == BI_BF16) return qgemm_bits<__nv_bfloat16>(bits, tx, tw, args, s);
-    if (dt == BI_F16) return qgemm_bits<__half>(bits, tx, tw, args, s);
+    {
+        // scales and biases: [N, K/group_size] at row stride ldsb; boxes of 8 groups
+        const uint64_t dims[2] = {static_cast<uint64_t>(args.K / args.group_size),
+                                  static_cast<uint64_t>(args.N)};
+        const uint64_t strides[1] = {static_cast<uint64_t>(args.ldsb) * 2};
+        const uint32_t box[2] = {8, QG_N};
+        bi_status st = encode_tmap(&ts, dt, 2, const_cast<void *>(args.scales), dims, strides,
+                                   box, false);
+        if (st != BI_OK) return st;
+        st = encode_tmap(&tb, dt, 2, const_cast<void *>(args.biases), dims, strides, box, false);
+        if (st != BI_OK) return st;
+    }
+    if (dt == BI_BF16) return qgemm_bits<__nv_bfloat16>(bits, tx, tw, ts, tb, args, s);
+    if (dt == BI_F16) return qgemm_bits<__half>(bits, tx, tw, ts, tb, args, s);
     return BI_ERR_UNSUPPORTED;
 }
 

@@ -3,6 +3,9 @@
   python -m attention_bi_matmul_gb300.profile_case linear M N K [--reps R]
   python -m attention_bi_matmul_gb300.profile_case matmul M N K [--reps R]
   python -m attention_bi_matmul_gb300.profile_case sdpa B H Hkv Lq Lkv [--reps R]
+  python -m attention_bi_matmul_gb300.profile_case qlinear M N K BITS GROUP [--reps R]
+      (bf16 activations; each call on one of 8 quantized weight copies, so the
+      packed weights come from HBM)
   python -m attention_bi_matmul_gb300.profile_case sweep [--reps R]
       (bf16 linear, K=4096, N in {4096, 11008, 14336}, M in {1,..,512}, each call
       on one of 4 weight copies, as in the benchmark's batch sweep)
@@ -26,7 +29,7 @@ if ROOT not in sys.path:
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("op", choices=("linear", "matmul", "sdpa", "sweep"))
+    ap.add_argument("op", choices=("linear", "matmul", "sdpa", "sweep", "qlinear"))
     ap.add_argument("dims", type=int, nargs="*")
     ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()
@@ -41,6 +44,19 @@ def main():
         y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         fn = (lambda: bi.linear(a, b, out=y)) if args.op == "linear" else (lambda: bi.matmul(a, b, out=y))
         work = "%.3f GFLOP" % (2.0 * M * N * K / 1e9)
+    elif args.op == "qlinear":
+        M, N, K, bits, gs = args.dims
+        x = synth.normal((M, K), 0, 1.0, "bf16", dev)
+        copies = [synth.qweights(N, K, bits, gs, "bf16", seed=i, device=dev) for i in range(8)]
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        state = {"i": 0}
+
+        def fn():
+            wq, sc, bs = copies[state["i"] % 8]
+            state["i"] += 1
+            bi.qlinear(x, wq, sc, bs, bits, gs, out=y)
+        nbytes = N * K * bits / 8 + 2 * 2 * N * K / gs + 2 * M * K + 2 * M * N
+        work = "%.4f GB (packed weights, scales, biases, x, y)" % (nbytes / 1e9)
     elif args.op == "sweep":
         Ns, Ms, K = (4096, 11008, 14336), (1, 2, 3, 4, 8, 16, 32, 64, 128, 256, 512), 4096
         x = synth.normal((512, K), 0, 1.0 / math.sqrt(K), "bf16", dev)

@@ -125,7 +125,8 @@ bi_status bi_matmul_batched(const void *a, int64_t lda, int64_t sa, const void *
  *            formed with one rounding to the activation dtype.
  *   x       device [M,K] bf16/fp16, leading dimension ldx >= K (multiple of 8)
  *   wq      device uint32 [N, ldq], ldq >= K*bits/32 (multiple of 4), 16-byte aligned
- *   scales, biases  device [N, ldsb] in x's dtype, ldsb >= K/group_size
+ *   scales, biases  device [N, ldsb] in x's dtype, ldsb >= K/group_size, a multiple
+ *           of 8 elements, 16-byte aligned (they are copied in 16-byte boxes)
  *   bias    device [N] or NULL; added to the fp32 accumulator, rounded once
  *   y       device [M,N], leading dimension ldy >= N
  *   bits in {2, 4, 8}; group_size in {32, 64, 128}; K a multiple of 64 and of

@@ -99,7 +99,7 @@ def test_qlinear_validation(lib):
 
     def call(bits=4, gs=64, K=256, ldq=None, ldx=256, dt=L.BI_BF16, ldsb=None, M=8, xp=p):
         ldq = K * bits // 32 if ldq is None else ldq
-        ldsb = K // gs if ldsb is None else ldsb
+        ldsb = max(8, K // gs) if ldsb is None else ldsb
         return lib.bi_qlinear(xp, ldx, p, ldq, p, p, ldsb, None, p, 64, M, 64, K, bits, gs, dt, s)
 
     assert call(bits=3) == L.BI_ERR_UNSUPPORTED               # 3-bit packing not built
@@ -109,6 +109,7 @@ def test_qlinear_validation(lib):
     assert call(K=192, ldx=192, gs=128) == L.BI_ERR_INVALID_ARG   # K not a multiple of gs
     assert call(ldq=16) == L.BI_ERR_INVALID_ARG                # row shorter than K*bits/32
     assert call(ldsb=3) == L.BI_ERR_INVALID_ARG
+    assert call(ldsb=12) == L.BI_ERR_ALIGNMENT                 # scale rows in 16-byte boxes
     assert call(ldq=34) == L.BI_ERR_ALIGNMENT                  # 16-byte rows for the copy
     assert call(xp=ctypes.c_void_p(4104)) == L.BI_ERR_ALIGNMENT
     assert call(M=0) == L.BI_OK

@@ -61,6 +61,23 @@ def test_ragged_shapes(bi, M, N):
     check_close(y, ref, nrm, torch.bfloat16, "qlinear M=%d N=%d" % (M, N))
 
 
+def test_unaligned_scale_rows_are_padded(bi):
+    """K / group_size = 172 groups (K = 11008): rows not a multiple of 8 elements take the
+    wrapper's padded copy and give the same bits as an aligned layout of the same values."""
+    M, N, K, bits, gs = 5, 256, 11008, 4, 64
+    x = synth.normal((M, K), 21, 1.0, "bf16").cuda()
+    wq, sc, bs = (t.cuda() for t in synth.qweights(N, K, bits, gs, "bf16", seed=22))
+    assert sc.stride(0) % 8 != 0
+    y = bi.qlinear(x, wq, sc, bs, bits, gs)
+    pad = torch.zeros((N, 2, 176), dtype=sc.dtype, device="cuda")
+    pad[:, 0, :172] = sc
+    pad[:, 1, :172] = bs
+    y2 = bi.qlinear(x, wq, pad[:, 0, :172], pad[:, 1, :172], bits, gs)
+    assert_same_bits(y, y2, "padded vs aligned scale rows")
+    ref, nrm = oracle.qlinear(x.cpu(), wq.cpu(), sc.cpu(), bs.cpu(), bits, gs)
+    check_close(y, ref, nrm, torch.bfloat16, "qlinear K=11008")
+
+
 @pytest.mark.parametrize("dt", ["bf16", "fp16"])
 @pytest.mark.parametrize("bits", [2, 4, 8])
 def test_dequantised_value_is_rounded_once(bi, dt, bits):
