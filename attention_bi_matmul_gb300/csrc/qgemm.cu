@@ -342,6 +342,7 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
         if (lane == 0) {
             // ------------------------------------------------ MMA issuer
             const uint64_t x_desc0 = smem_desc(smem_u32(sX), 16, 1024);
+            const uint64_t xb16 = XB >> 4;          // one x panel in descriptor units
             uint32_t tc = 0, xph = 0, d = 0, dph = 0;
             int xs = 0;
             bool ok = true;
@@ -360,16 +361,12 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
                     tc_fence_after();
                     const uint32_t a_tmem = tmem_base + QG_A_COL + d * QB_B * (QG_K / 2);
                     const uint64_t xd = x_desc0 + ((xs * XBB) >> 4);
+                    // panel b: A columns a_tmem + 32 b (8 per 16 k), x panel b of the batch
+                    mma4_f16_ts(d_tmem, a_tmem, xd, IDESC, p0 != 0 ? 1u : 0u);
 #pragma unroll
-                    for (int b = 0; b < QB_B; ++b) {
-                        if (b < nb_) {
-#pragma unroll
-                            for (int j = 0; j < QG_K / 16; ++j)   // 16 k = 8 columns of A
-                                mma_f16_ts(d_tmem, a_tmem + b * (QG_K / 2) + j * 8,
-                                           xd + ((b * XB) >> 4) + j * (32 >> 4), IDESC,
-                                           (p0 + b + j) != 0 ? 1u : 0u);
-                        }
-                    }
+                    for (int b = 1; b < QB_B; ++b)
+                        if (b < nb_)
+                            mma4_f16_ts(d_tmem, a_tmem + b * (QG_K / 2), xd + b * xb16, IDESC, 1u);
                     mma_commit(&a_empty[d]);
                     mma_commit(&x_empty[xs]);
                     if (++d == DSB) { d = 0; dph ^= 1u; }
