@@ -114,18 +114,25 @@ __host__ __device__ constexpr uint32_t tc_tmem_cols(int bn) {
            : (2 * bn <= 256) ? 256u : 512u;
 }
 
-// Pipeline shape per tile width, 192 KB of shared memory in both cases:
+// Pipeline shape per tile width, 192 KB of shared memory in both cases (with
+// 128-row A panels; fewer A rows leave room for more stages, see the kernel):
 //   128 columns: stages of 2 K panels (8 MMAs of 64 cycles per barrier round trip), 3 stages;
 //   256 columns: stages of 1 K panel (4 MMAs of 128 cycles), 4 stages.
 template <int BN> __host__ __device__ constexpr int tc_kp() { return BN <= 128 ? 2 : 1; }
 template <int BN> __host__ __device__ constexpr int tc_stages() { return BN <= 128 ? 3 : 4; }
 template <int BN> __host__ __device__ constexpr bool tc_l2_prefetch() { return BN <= 128; }
 
+// Ring bytes: tc_stages stages of full 128-row A panels.  With fewer A rows a
+// stage is smaller and the same bytes hold more stages (up to TC_MAX_STAGES).
+constexpr int TC_MAX_STAGES = 16;
+template <int BN>
+__host__ __device__ constexpr uint32_t tc_ring_bytes() {
+    return (uint32_t)tc_stages<BN>() * tc_kp<BN>() * (TC_BM * TC_BK * 2 + BN * TC_BK * 2);
+}
 template <int BN>
 __host__ __device__ constexpr size_t tc_smem_bytes() {
-    return 1024 /* alignment slack */ +
-           (size_t)tc_stages<BN>() * tc_kp<BN>() * (TC_BM * TC_BK * 2 + BN * TC_BK * 2) +
-           256 /* barriers etc */;
+    return 1024 /* alignment slack */ + tc_ring_bytes<BN>() +
+           (2 * TC_MAX_STAGES + 5) * 8 + 16 /* barriers, TMEM slot, abort flag */;
 }
 
 // Tile t -> (batch entry, m block, n block); within an entry, tiles are grouped so
@@ -148,11 +155,9 @@ template <typename T, int BN, bool B_MN>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmArgs args) {
-    constexpr int KP = tc_kp<BN>(), STAGES = tc_stages<BN>();
-    constexpr uint32_t A_PANEL = TC_BM * TC_BK * 2;   // 16 KB
+    constexpr int KP = tc_kp<BN>();
     constexpr uint32_t B_PANEL = BN * TC_BK * 2;
-    constexpr uint32_t A_BYTES = KP * A_PANEL;        // per stage
-    constexpr uint32_t B_BYTES = KP * B_PANEL;
+    constexpr uint32_t B_BYTES = KP * B_PANEL;        // per stage
     constexpr uint32_t TMEM_COLS = tc_tmem_cols(BN);
     constexpr uint32_t IDESC = mma_idesc(IsBf16<T>::value, TC_BM, BN, B_MN);
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile width");
@@ -161,11 +166,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
+    // Ring layout for this call: A panels hold the a_rows rows the copy moves (a
+    // multiple of 16 rows, so every panel starts on the 1024-byte swizzle period),
+    // then the B panels.  The MMA always reads 128 A rows; rows past a_rows hold
+    // whatever follows (the next panel, or the first B panels) and only feed tile
+    // rows that are never stored.  Fewer A rows -> more stages in the same bytes;
+    // the ring depth changes only the scheduling, never the order of any MMA.
+    const uint32_t A_PANEL = static_cast<uint32_t>(args.a_rows) * TC_BK * 2;
+    const uint32_t A_BYTES = KP * A_PANEL;            // per stage
+    const uint32_t ST_FIT = tc_ring_bytes<BN>() / (A_BYTES + B_BYTES);
+    const int STAGES = static_cast<int>(ST_FIT < TC_MAX_STAGES ? ST_FIT : TC_MAX_STAGES);
     uint8_t *sA = smem;
     uint8_t *sB = smem + STAGES * A_BYTES;
-    uint64_t *full = reinterpret_cast<uint64_t *>(sB + STAGES * B_BYTES);
-    uint64_t *empty = full + STAGES;
-    uint64_t *tfull = empty + STAGES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + tc_ring_bytes<BN>());
+    uint64_t *empty = full + TC_MAX_STAGES;
+    uint64_t *tfull = empty + TC_MAX_STAGES;
     uint64_t *tempty = tfull + 2;
     uint64_t *mma_done = tempty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
@@ -212,6 +227,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const uint32_t tx = KP * (static_cast<uint32_t>(args.a_rows) * TC_BK * 2 + B_PANEL);
             uint32_t it = 0, s = 0, ph = 0;
             bool ok = true;
+            auto prefetch_stage = [&](int kq_stage, int64_t nb, int32_t eb) {
+#pragma unroll
+                for (int p = 0; p < KP; ++p) {
+                    const int32_t kq = (kq_stage * KP + p) * TC_BK;
+                    if (!B_MN) {
+                        tma_prefetch_3d(&tmB, kq, static_cast<int32_t>(nb * BN), eb);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < BN / 64; ++j)
+                            tma_prefetch_3d(&tmB, static_cast<int32_t>(nb * BN + j * 64), kq, eb);
+                    }
+                }
+            };
             for (int64_t t = blockIdx.x; ok && t < total; t += gridDim.x) {
                 int64_t e, mb, nb;
                 tc_tile_coords(t, num_m, num_n, e, mb, nb);
@@ -237,30 +265,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                             eb);
                         }
                     }
-                    // 128-column tiles stream their weight panels from HBM with a short
-                    // ring; ask for the panels one ring further on to move into L2 now.
-                    // (Measured: +2-5% for those; it costs the L2-resident 256-wide
-                    // tiles 7%, so they do not.)
-                    if (tc_l2_prefetch<BN>() && kb + STAGES < KB) {
-#pragma unroll
-                        for (int p = 0; p < KP; ++p) {
-                            const int32_t kq = ((kb + STAGES) * KP + p) * TC_BK;
-                            if (!B_MN) {
-                                tma_prefetch_3d(&tmB, kq, static_cast<int32_t>(nb * BN), eb);
-                            } else {
-#pragma unroll
-                                for (int j = 0; j < BN / 64; ++j)
-                                    tma_prefetch_3d(&tmB, static_cast<int32_t>(nb * BN + j * 64),
-                                                    kq, eb);
-                            }
-                        }
-                    }
+                    // 128-column tiles stream their weight panels from HBM; ask for the
+                    // panels one ring further on to move into L2 now.  (Measured: +2-5%
+                    // for those; it costs the L2-resident 256-wide tiles 7%, so they do
+                    // not.  Prefetching further ahead was slower.)
+                    if (tc_l2_prefetch<BN>() && kb + STAGES < KB) prefetch_stage(kb + STAGES, nb, eb);
                     if (++s == STAGES) { s = 0; ph ^= 1u; }
                 }
             }
             if (!ok) {
                 // Let every copy already issued land before the block can exit.
-                const uint32_t first = it > STAGES ? it - STAGES : 0;
+                const uint32_t first = it > static_cast<uint32_t>(STAGES) ? it - STAGES : 0;
                 for (uint32_t i = first; i < it; ++i)
                     mbar_wait_limited(&full[i % STAGES], (i / STAGES) & 1u, WAIT_LIMIT_NS);
             }
@@ -274,8 +289,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const uint64_t a_desc0 = smem_desc(smem_u32(sA), 16, 1024);
             const uint64_t b_desc0 = B_MN ? smem_desc(smem_u32(sB), 8192, 1024)
                                           : smem_desc(smem_u32(sB), 16, 1024);
-            constexpr uint64_t A_STEP = A_BYTES >> 4, B_STEP = B_BYTES >> 4;
-            constexpr uint64_t AP_STEP = A_PANEL >> 4, BP_STEP = B_PANEL >> 4;
+            const uint64_t A_STEP = A_BYTES >> 4, AP_STEP = A_PANEL >> 4;
+            constexpr uint64_t B_STEP = B_BYTES >> 4, BP_STEP = B_PANEL >> 4;
             constexpr uint64_t BK_STEP = B_MN ? (2048 >> 4) : (32 >> 4);
             uint32_t tc = 0, s = 0, ph = 0;
             bool ok = true;
