@@ -120,6 +120,7 @@ bi_status device_init(int dev) {
     if ((st = init_gemm_tc_f16()) != BI_OK) return st;
     if ((st = init_sdpa()) != BI_OK) return st;
     if ((st = init_qgemm()) != BI_OK) return st;
+    if ((st = init_sdpa256()) != BI_OK) return st;
     if (!device_error_word()) return BI_ERR_CUDA;
     device_sm_count();
     if (!load_encode()) return BI_ERR_CUDA;
@@ -389,7 +390,8 @@ bi_status bi_sdpa_ex(const void *q, const int64_t qs[4], const void *k, const in
     if (q_offset < 0 || (mask == BI_MASK_CAUSAL && q_offset + Lq > Lkv)) return BI_ERR_INVALID_ARG;
     if (Lq == 0 || B == 0) return BI_OK;
     if (Lkv == 0) return BI_ERR_INVALID_ARG;   // no key at all
-    if (D != 64 && D != 96 && D != 128) return BI_ERR_UNSUPPORTED;
+    if (D != 64 && D != 96 && D != 128 && D != 160 && D != 192 && D != 224 && D != 256)
+        return BI_ERR_UNSUPPORTED;
     const int64_t G = H / Hkv;
     if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return BI_ERR_UNSUPPORTED;
     if (qs[3] != 1 || ks[3] != 1 || vs[3] != 1 || os[3] != 1) return BI_ERR_INVALID_ARG;
@@ -408,7 +410,7 @@ bi_status bi_sdpa_ex(const void *q, const int64_t qs[4], const void *k, const in
     a.group = static_cast<int>(G);
     a.qt = static_cast<int>(128 / G);
     a.D = static_cast<int>(D);
-    a.dp = D <= 64 ? 64 : 128;
+    a.dp = D <= 64 ? 64 : D <= 128 ? 128 : 256;
     a.mode = mask == BI_MASK_CAUSAL ? 1 : mask == BI_MASK_ARRAY ? 2 : 0;
     const double sc = scale > 0.0f ? static_cast<double>(scale) : 1.0 / std::sqrt(static_cast<double>(D));
     a.scale_log2 = static_cast<float>(sc * 1.4426950408889634);   // scale * log2(e)
@@ -434,7 +436,8 @@ bi_status bi_sdpa_ex(const void *q, const int64_t qs[4], const void *k, const in
     {
         const uint64_t dims[4] = {static_cast<uint64_t>(D), static_cast<uint64_t>(Lkv),
                                   static_cast<uint64_t>(Hkv), static_cast<uint64_t>(B)};
-        const uint32_t box[4] = {64, 128, 1, 1};
+        // key chunks of 128 (head dims up to 128) or 64 (the 256-column kernel)
+        const uint32_t box[4] = {64, a.dp == 256 ? 64u : 128u, 1, 1};
         const uint64_t sk[3] = {static_cast<uint64_t>(ks[2]) * 2, static_cast<uint64_t>(ks[1]) * 2,
                                 static_cast<uint64_t>(ks[0]) * 2};
         st = encode_tmap(&tk, dtype, 4, const_cast<void *>(k), dims, sk, box, true);

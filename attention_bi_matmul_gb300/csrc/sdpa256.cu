@@ -1,0 +1,422 @@
+// sdpa256.cu -- batch-invariant attention at head dims 160..256 (a 256-column
+// tile) on the 5th-generation tensor cores, the output accumulated in tensor
+// memory.
+//
+// "mlx-batch-invariant" README, "How the kernels work" / Attention (single pass
+// over the keys in a fixed order, online softmax in fp32, no split over the
+// keys) and the closing limits paragraph (head dims are multiples of 32).  The
+// rule of the 128-wide kernel holds; what changes with the head dim:
+//
+//   * keys are visited in chunks of 64 at absolute positions 0, 64, 128, ...;
+//     S = Q K^T takes 16 K = 16 steps per chunk;
+//   * the output is one fp32 accumulator in tensor memory that the P V MMA adds
+//     into: before chunk j's P V, every row rescales it by
+//     alpha_j = 2^(m_{j-1} - m_j) (one fp32 multiply per element, rounded to
+//     nearest), then the MMA adds P_j V_j.  A warp whose 32 rows all have
+//     alpha = 1 skips the rescale: multiplying by 1 is exact, so the bits do
+//     not depend on which rows share the warp;
+//   * a chunk entirely masked for a row has alpha = 1 and p = 0: the rescale and
+//     the added zeros leave its accumulator unchanged, so extra chunks that a
+//     longer query tile visits, or keys appended past a token, change nothing;
+//   * o = acc / l (IEEE division), rounded once.
+// Query tiles, rows, masks and sinks are as in the 128-wide kernel.
+//
+// Roles (320 threads):
+//   warp 0 lane 0   TMA producer (Q once; K and V chunks of 64 keys through
+//                   2-deep rings)
+//   warp 1          TMEM allocation (512 columns: S0, S1 of 64, O of 256);
+//                   lane 0 issues the MMAs
+//   warps 2..9      row warps: warp w serves TMEM lane quarter w % 4 and half
+//                   (w-2)/4 of the keys (32) and of the output columns (128).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "gemm_tc.cuh"  // IsBf16 / pack8
+#include "internal.cuh"
+#include "ptx.cuh"
+#include "sdpa_common.cuh"
+
+namespace bi {
+
+namespace {
+
+constexpr int S2_C = 64;           // keys per chunk
+constexpr int S2_ROWS = 128;       // rows per query tile
+constexpr int S2_DP = 256;         // padded head dim
+constexpr int S2_KST = 2;          // K ring depth
+constexpr int S2_VST = 2;          // V ring depth
+constexpr int S2_THREADS = 320;
+constexpr uint32_t S2_QPANEL = S2_ROWS * 128;     // 16 KB: 128 rows x 64 elements
+constexpr uint32_t S2_KPANEL = S2_C * 128;        // 8 KB: 64 keys x 64 elements
+constexpr uint32_t S2_Q = 4 * S2_QPANEL;          // 64 KB
+constexpr uint32_t S2_KV = 4 * S2_KPANEL;         // 32 KB per chunk
+constexpr uint32_t S2_P = S2_ROWS * 128;          // 16 KB: 128 rows x 64 keys
+constexpr uint32_t S2_TMEM_COLS = 512;            // S0 [0,64) S1 [64,128) O [128,384)
+constexpr uint32_t S2_O_COL = 128;
+
+struct S2Smem {
+    static constexpr uint32_t Q = 0;
+    static constexpr uint32_t K = Q + S2_Q;
+    static constexpr uint32_t V = K + S2_KST * S2_KV;
+    static constexpr uint32_t P = V + S2_VST * S2_KV;
+    static constexpr uint32_t MX = P + S2_P;                     // float[2][128] half maxima
+    static constexpr uint32_t LS = MX + 2 * 128 * 4;             // float[2][128] half sums
+    static constexpr uint32_t BARS = LS + 2 * 128 * 4;
+    // bar_q kfull[2] kempty[2] vfull[2] vempty[2] sfull[2] sempty[2] pfull pvdone mma_done
+    static constexpr uint32_t NBARS = 1 + 2 * S2_KST + 2 * S2_VST + 4 + 3;
+    static constexpr uint32_t MISC = BARS + NBARS * 8;           // tmem slot, abort flag
+    static constexpr uint32_t END = MISC + 16;
+    static constexpr size_t BYTES = 1024 + END;
+};
+
+template <typename T, bool ARR>
+__global__ void __launch_bounds__(S2_THREADS, 1)
+    sdpa256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const SdpaArgs args) {
+    constexpr uint32_t IDESC_S = mma_idesc(IsBf16<T>::value, S2_ROWS, S2_C, false);
+    constexpr uint32_t IDESC_PV = mma_idesc(IsBf16<T>::value, S2_ROWS, S2_DP, true);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    uint8_t *sQ = smem + S2Smem::Q;
+    uint8_t *sK = smem + S2Smem::K;
+    uint8_t *sV = smem + S2Smem::V;
+    uint8_t *sP = smem + S2Smem::P;
+    float *mx_s = reinterpret_cast<float *>(smem + S2Smem::MX);
+    float *ls_s = reinterpret_cast<float *>(smem + S2Smem::LS);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S2Smem::BARS);
+    uint64_t *bar_q = bars;
+    uint64_t *kfull = bar_q + 1;
+    uint64_t *kempty = kfull + S2_KST;
+    uint64_t *vfull = kempty + S2_KST;
+    uint64_t *vempty = vfull + S2_VST;
+    uint64_t *sfull = vempty + S2_VST;   // [2]
+    uint64_t *sempty = sfull + 2;        // [2]
+    uint64_t *pfull = sempty + 2;        // P_j in smem and O rescaled for chunk j
+    uint64_t *pvdone = pfull + 1;        // P_j V_j added into O (P free, O readable)
+    uint64_t *mma_done = pvdone + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S2Smem::MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S2Smem::MISC + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    const int G = args.group;
+    const int Qt = args.qt;
+    const int64_t q_offset = args.q_offset;
+    const int64_t Lq = args.Lq, Lkv = args.Lkv;
+    // Query tiles of this call, heaviest (latest positions) first.
+    const int64_t t_last = (q_offset + Lq - 1) / Qt;
+    const int64_t tile = t_last - static_cast<int64_t>(blockIdx.x);
+    const int kvh = static_cast<int>(blockIdx.y);
+    const int b = static_cast<int>(blockIdx.z);
+    const int64_t p_lo = tile * Qt;
+    int64_t p_max = p_lo + Qt - 1;
+    if (p_max > q_offset + Lq - 1) p_max = q_offset + Lq - 1;
+    const int nchunks = args.mode == 1 ? static_cast<int>(p_max / S2_C + 1)
+                                       : static_cast<int>((Lkv + S2_C - 1) / S2_C);
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar_q, 1);
+        for (int s = 0; s < S2_KST; ++s) { mbar_init(&kfull[s], 1); mbar_init(&kempty[s], 1); }
+        for (int s = 0; s < S2_VST; ++s) { mbar_init(&vfull[s], 1); mbar_init(&vempty[s], 1); }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sfull[i], 1);
+            mbar_init(&sempty[i], 8);
+        }
+        mbar_init(pfull, 8);
+        mbar_init(pvdone, 1);
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, S2_TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            prefetch_tmap(&tmQ);
+            prefetch_tmap(&tmK);
+            prefetch_tmap(&tmV);
+            const int32_t qi0 = static_cast<int32_t>(p_lo - q_offset);  // may be negative
+            mbar_arrive_expect_tx(bar_q, S2_Q);
+#pragma unroll
+            for (uint32_t pn = 0; pn < 4; ++pn)
+                tma_load_4d(sQ + pn * S2_QPANEL, &tmQ, bar_q, 64 * pn, kvh * G, qi0, b);
+            int armed = 0;
+            bool ok = true;
+            for (int j = 0; j < nchunks; ++j) {
+                const uint32_t sk = j % S2_KST, phk = (j / S2_KST) & 1u;
+                if (!mbar_wait(&kempty[sk], phk ^ 1u, abort_flag)) { ok = false; break; }
+                mbar_arrive_expect_tx(&kfull[sk], S2_KV);
+#pragma unroll
+                for (uint32_t pn = 0; pn < 4; ++pn)
+                    tma_load_4d(sK + sk * S2_KV + pn * S2_KPANEL, &tmK, &kfull[sk], 64 * pn,
+                                j * S2_C, kvh, b);
+                const uint32_t sv = j % S2_VST, phv = (j / S2_VST) & 1u;
+                if (!mbar_wait(&vempty[sv], phv ^ 1u, abort_flag)) { ok = false; armed = 2 * j + 1; break; }
+                mbar_arrive_expect_tx(&vfull[sv], S2_KV);
+#pragma unroll
+                for (uint32_t pn = 0; pn < 4; ++pn)
+                    tma_load_4d(sV + sv * S2_KV + pn * S2_KPANEL, &tmV, &vfull[sv], 64 * pn,
+                                j * S2_C, kvh, b);
+                armed = 2 * j + 2;
+            }
+            if (!ok) {
+                // Let every copy already issued land before the block can exit.
+                mbar_wait_limited(bar_q, 0, WAIT_LIMIT_NS);
+                const int nk = (armed + 1) / 2, nv = armed / 2;
+                for (int j = nk - S2_KST < 0 ? 0 : nk - S2_KST; j < nk; ++j)
+                    mbar_wait_limited(&kfull[j % S2_KST], (j / S2_KST) & 1u, WAIT_LIMIT_NS);
+                for (int j = nv - S2_VST < 0 ? 0 : nv - S2_VST; j < nv; ++j)
+                    mbar_wait_limited(&vfull[j % S2_VST], (j / S2_VST) & 1u, WAIT_LIMIT_NS);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            bool ok = mbar_wait(bar_q, 0, abort_flag);
+            const uint32_t q_addr = smem_u32(sQ);
+            const uint32_t p_addr = smem_u32(sP);
+            for (int j = 0; ok && j <= nchunks; ++j) {
+                if (j < nchunks) {
+                    // S(j) = Q K_j^T into S buffer j & 1 (16 K = 16 steps over the head dim)
+                    const uint32_t sk = j % S2_KST;
+                    const uint32_t sb = j & 1;
+                    if (!mbar_wait(&kfull[sk], (j / S2_KST) & 1u, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(&sempty[sb], ((j >> 1) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t k_addr = smem_u32(sK + sk * S2_KV);
+#pragma unroll
+                    for (int kk = 0; kk < S2_DP / 16; ++kk) {
+                        mma_f16_ss(tmem_base + sb * S2_C,
+                                   smem_desc(q_addr + (kk >> 2) * S2_QPANEL + (kk & 3) * 32, 16, 1024),
+                                   smem_desc(k_addr + (kk >> 2) * S2_KPANEL + (kk & 3) * 32, 16, 1024),
+                                   IDESC_S, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&kempty[sk]);
+                    mma_commit(&sfull[sb]);
+                }
+                if (j >= 1) {
+                    // O (+)= P_i V_i, i = j - 1 (the rows rescaled O before signalling)
+                    const int i = j - 1;
+                    const uint32_t sv = i % S2_VST;
+                    if (!mbar_wait(pfull, i & 1u, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(&vfull[sv], (i / S2_VST) & 1u, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t v_addr = smem_u32(sV + sv * S2_KV);
+#pragma unroll
+                    for (int kk = 0; kk < S2_C / 16; ++kk) {
+                        mma_f16_ss(tmem_base + S2_O_COL, smem_desc(p_addr + kk * 32, 16, 1024),
+                                   smem_desc(v_addr + kk * 2048, S2_KPANEL, 1024), IDESC_PV,
+                                   (i > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    mma_commit(&vempty[sv]);
+                    mma_commit(pvdone);
+                }
+            }
+            mma_commit(mma_done);
+            mbar_wait_limited(mma_done, 0, WAIT_LIMIT_NS);
+        }
+    } else {
+        // ------------------------------------------------ row warps (2..9)
+        // As in the 128-wide kernel these warps never leave the chunk loop early, so
+        // the two warps of a lane quarter always meet at the same named barriers.
+        const uint32_t quarter = static_cast<uint32_t>(warp & 3);
+        const int half = (warp - 2) >> 2;   // keys 32*half..+31; output columns 128*half..+127
+        const int r = static_cast<int>(quarter) * 32 + lane;
+        const int qi = r / G, g = r - (r / G) * G;
+        const int64_t pos = p_lo + qi;
+        const bool valid = pos >= q_offset && pos < q_offset + Lq;
+        const bool warp_valid = __any_sync(0xffffffffu, valid) != 0;
+        const uint32_t lane_base = (quarter * 32u) << 16;
+        const float sl2 = args.scale_log2;
+        const int h = kvh * G + g;
+        int64_t vis_end = args.mode == 1 ? pos + 1 : Lkv;
+        if (vis_end > Lkv) vis_end = Lkv;
+        if (!valid) vis_end = INT64_MAX / 2;
+        const uint8_t *mrow = nullptr;
+        if (ARR && valid)
+            mrow = args.mask + b * args.ms[0] + h * args.ms[1] + (pos - q_offset) * args.ms[2];
+        float m_run = -INFINITY, l_run = 0.0f;
+        if (args.sinks) {
+            m_run = __fmul_rn(args.sinks[h], 1.44269504088896341f);
+            l_run = 1.0f;
+        }
+        const uint32_t o_addr = tmem_base + lane_base + S2_O_COL + half * 128;
+
+        for (int j = 0; j < nchunks; ++j) {
+            const uint32_t sb = j & 1;
+            const int64_t key0 = static_cast<int64_t>(j) * S2_C + half * 32;
+            uint32_t vis = ~0u;
+            if (ARR && mrow) vis = mask_bits32(mrow + key0, Lkv - key0);
+            warp_wait(&sfull[sb], (j >> 1) & 1u, abort_flag);
+            tc_fence_after();
+            int lim = 32;
+            if (!ARR) {
+                const int64_t lim64 = vis_end - key0;
+                lim = lim64 < 0 ? 0 : (lim64 > 32 ? 32 : static_cast<int>(lim64));
+            }
+            const bool full = __all_sync(0xffffffffu, ARR ? vis == ~0u : lim == 32) != 0;
+            float x[32];
+            float mloc = -INFINITY;
+            if (warp_valid) {
+                uint32_t(&xu)[32] = *reinterpret_cast<uint32_t(*)[32]>(x);
+                tmem_ld32(tmem_base + lane_base + sb * S2_C + half * 32, xu);
+                tmem_wait_ld(xu);
+                if (full) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) mloc = fmaxf(mloc, x[i]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (ARR ? ((vis >> i) & 1u) != 0 : i < lim) mloc = fmaxf(mloc, x[i]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sempty[sb]);
+            mx_s[half * 128 + r] = mloc;
+            pair_sync(quarter);
+            const float mraw = fmaxf(mx_s[r], mx_s[128 + r]);
+            const bool any = mraw != -INFINITY;
+            const float m_new = any ? fmaxf(m_run, __fmul_rn(mraw, sl2)) : m_run;
+            const float alpha = any ? ex2_approx(__fsub_rn(m_run, m_new)) : 1.0f;
+            float ls4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            if (warp_valid) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    float e = ex2_approx(__fmaf_rn(x[i], sl2, -m_new));
+                    if (!full && (ARR ? ((vis >> i) & 1u) == 0 : i >= lim)) e = 0.0f;
+                    x[i] = e;
+                    ls4[i & 3] = __fadd_rn(ls4[i & 3], e);
+                }
+            }
+            const float lsum = __fadd_rn(__fadd_rn(ls4[0], ls4[1]), __fadd_rn(ls4[2], ls4[3]));
+            // P_j and the rescaled O must wait until P_{j-1} V_{j-1} is added in
+            if (j >= 1) {
+                warp_wait(pvdone, (j - 1) & 1u, abort_flag);
+                tc_fence_after();
+            }
+            if (warp_valid) {
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const uint4 v = pack8x2<T>(x + cc * 8);
+                    uint8_t *dst = sP + r * 128 + (((half * 4 + cc) ^ (r & 7)) << 4);
+                    *reinterpret_cast<uint4 *>(dst) = v;
+                }
+                fence_proxy_async_smem();
+                // O *= alpha for this warp's 128 columns (skipped when every row has alpha 1)
+                if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+#pragma unroll 1
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        uint32_t ov[32];
+                        tmem_ld32(o_addr + c4 * 32, ov);
+                        tmem_wait_ld(ov);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            ov[e] = __float_as_uint(__fmul_rn(__uint_as_float(ov[e]), alpha));
+                        tmem_st32(o_addr + c4 * 32, ov);
+                    }
+                    tmem_wait_st();
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(pfull);
+            ls_s[half * 128 + r] = lsum;
+            pair_sync(quarter);
+            if (any) {
+                l_run = __fadd_rn(__fmul_rn(l_run, alpha), __fadd_rn(ls_s[r], ls_s[128 + r]));
+                m_run = m_new;
+            }
+        }
+        // the last P V, then o = acc / l
+        warp_wait(pvdone, (nchunks - 1) & 1u, abort_flag);
+        tc_fence_after();
+        if (warp_valid) {
+            T *orow = static_cast<T *>(args.o) + b * args.os[0] + h * args.os[1] +
+                      (pos - q_offset) * args.os[2] + half * 128;
+#pragma unroll 1
+            for (int c4 = 0; c4 < 4; ++c4) {
+                uint32_t ov[32];
+                tmem_ld32(o_addr + c4 * 32, ov);
+                tmem_wait_ld(ov);
+                if (valid && !*abort_flag) {
+#pragma unroll
+                    for (int d8 = 0; d8 < 4; ++d8) {
+                        const int col = half * 128 + c4 * 32 + d8 * 8;
+                        if (col >= args.D) break;        // padded columns past the head dim
+                        float v[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            v[e] = __fdiv_rn(__uint_as_float(ov[d8 * 8 + e]), l_run);
+                        *reinterpret_cast<uint4 *>(orow + c4 * 32 + d8 * 8) = pack8<T>(v);
+                    }
+                }
+            }
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, S2_TMEM_COLS);
+    }
+    if (threadIdx.x == 0 && *abort_flag) atomicOr(args.err, ERR_TIMEOUT);
+}
+
+template <typename T, bool ARR>
+bi_status s2_attr() {
+    return cuda_status(cudaFuncSetAttribute(sdpa256_kernel<T, ARR>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            static_cast<int>(S2Smem::BYTES)));
+}
+
+template <typename T, bool ARR>
+bi_status s2_launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                    const SdpaArgs &args, cudaStream_t s) {
+    const int64_t t_first = args.q_offset / args.qt;
+    const int64_t t_last = (args.q_offset + args.Lq - 1) / args.qt;
+    const int64_t tiles = t_last - t_first + 1;
+    if (tiles > 0x7fffffff || args.Hkv > 65535 || args.B > 65535) return BI_ERR_UNSUPPORTED;
+    dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(args.Hkv),
+              static_cast<unsigned>(args.B));
+    sdpa256_kernel<T, ARR><<<grid, S2_THREADS, S2Smem::BYTES, s>>>(tq, tk, tv, args);
+    count_launch();
+    return cuda_status(cudaGetLastError());
+}
+
+}  // namespace
+
+bi_status init_sdpa256() {
+    bi_status (*const fns[])() = {s2_attr<__nv_bfloat16, false>, s2_attr<__nv_bfloat16, true>,
+                                  s2_attr<__half, false>, s2_attr<__half, true>};
+    for (auto f : fns) {
+        const bi_status st = f();
+        if (st != BI_OK) return st;
+    }
+    return BI_OK;
+}
+
+bi_status launch_sdpa256(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                         const SdpaArgs &args, bi_dtype dt, cudaStream_t s) {
+    const bool arr = args.mode == 2;
+    if (dt == BI_BF16)
+        return arr ? s2_launch<__nv_bfloat16, true>(tq, tk, tv, args, s)
+                   : s2_launch<__nv_bfloat16, false>(tq, tk, tv, args, s);
+    if (dt == BI_F16)
+        return arr ? s2_launch<__half, true>(tq, tk, tv, args, s)
+                   : s2_launch<__half, false>(tq, tk, tv, args, s);
+    return BI_ERR_UNSUPPORTED;
+}
+
+}  // namespace bi

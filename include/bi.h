@@ -167,7 +167,10 @@ bi_status bi_gemm_config(int64_t N, int64_t K, bi_dtype dtype, int b_layout, int
  *   absolute positions; a fully masked chunk is an exact no-op.  Hence a
  *   token's output bits do not depend on Lq, B, batch neighbours, or keys
  *   appended after it.  Masked keys must hold finite values.
- *   Built: dtype BI_BF16 / BI_F16, D = 128, H/Hkv in {1,2,4,8,16}.
+ *   Built: dtype BI_BF16 / BI_F16, D in {64, 96, 128, 160, 192, 224, 256} (96 and
+ *   160-224 run the 128- or 256-column kernel with the columns past D zero), H/Hkv
+ *   in {1,2,4,8,16}.  D up to 128 visits keys in chunks of 128, larger D in chunks
+ *   of 64: the chunking is a function of D alone.
  *   Lq == 0 or B == 0 is a no-op (BI_OK). */
 bi_status bi_sdpa(const void *q, const int64_t qs[4], const void *k, const int64_t ks[4],
                   const void *v, const int64_t vs[4], void *o, const int64_t os[4], int64_t B,

@@ -133,7 +133,7 @@ def test_sdpa_validation(lib):
     assert call(mask=5) == L.BI_ERR_UNSUPPORTED
     assert call(dt=L.BI_F32) == L.BI_ERR_UNSUPPORTED
     assert call(D=80) == L.BI_ERR_UNSUPPORTED                 # head dim not built
-    assert call(D=256) == L.BI_ERR_UNSUPPORTED
+    assert call(D=288) == L.BI_ERR_UNSUPPORTED
     assert call(D=32) == L.BI_ERR_UNSUPPORTED
     # Without the causal rule the positions only align the tiles: more queries than
     # keys pass validation; no keys at all do not.

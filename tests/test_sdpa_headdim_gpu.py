@@ -1,5 +1,7 @@
-"""Attention at head dims 64 and 96 (the kernel's 64- and 128-column forms; 96 is loaded
-with zero fill past the head dim): parity with the fp64 oracle and invariance."""
+"""Attention at head dims 64, 96, 160, 192 and 256 (the kernel's 64-, 128- and 256-column
+forms; 96 and 160-224 are loaded with zero fill past the head dim; the 256-column form
+keeps the output in tensor memory and visits keys in chunks of 64): parity with the fp64
+oracle and invariance."""
 import pytest
 import torch
 
@@ -27,7 +29,7 @@ def _no_device_error(bi):
 
 
 @pytest.mark.parametrize("dt", ["bf16", "fp16"])
-@pytest.mark.parametrize("D", [64, 96])
+@pytest.mark.parametrize("D", [64, 96, 160, 192, 256])
 @pytest.mark.parametrize("G", [1, 4, 16])
 def test_parity_head_dims(bi, dt, D, G):
     Hkv = 2
@@ -39,8 +41,9 @@ def test_parity_head_dims(bi, dt, D, G):
     _no_device_error(bi)
 
 
-@pytest.mark.parametrize("D", [64, 96])
-@pytest.mark.parametrize("Lq,Lkv,off", [(1, 1, 0), (1, 4097, 4096), (130, 130, 0), (7, 900, 500)])
+@pytest.mark.parametrize("D", [64, 96, 192, 256])
+@pytest.mark.parametrize("Lq,Lkv,off", [(1, 1, 0), (1, 4097, 4096), (130, 130, 0), (7, 900, 500),
+                                        (65, 65, 0), (1, 63, 62)])
 def test_parity_shapes_head_dims(bi, D, Lq, Lkv, off):
     q, k, v = synth.sdpa_qkv(1, 8, 2, Lq, Lkv, D, "bf16", seed=Lq + Lkv + D)
     o = bi.sdpa(q.cuda(), k.cuda(), v.cuda(), causal=True, q_offset=off)
@@ -48,7 +51,7 @@ def test_parity_shapes_head_dims(bi, D, Lq, Lkv, off):
     check_close(o, ref, nrm, torch.bfloat16, "sdpa D=%d Lq=%d Lkv=%d" % (D, Lq, Lkv))
 
 
-@pytest.mark.parametrize("D", [64, 96])
+@pytest.mark.parametrize("D", [64, 96, 160, 256])
 def test_mask_and_sinks_head_dims(bi, D):
     B, H, Hkv, Lq, Lkv = 2, 8, 2, 40, 700
     q, k, v = synth.sdpa_qkv(B, H, Hkv, Lq, Lkv, D, "bf16", seed=3 * D)
@@ -60,7 +63,7 @@ def test_mask_and_sinks_head_dims(bi, D):
     check_close(o, ref, nrm, torch.bfloat16, "sdpa D=%d mask + sinks" % D)
 
 
-@pytest.mark.parametrize("D", [64, 96])
+@pytest.mark.parametrize("D", [64, 96, 160, 256])
 def test_single_visible_key_is_exact_head_dims(bi, D):
     q, k, v = synth.sdpa_qkv(1, 4, 1, 1, 50, D, "bf16", seed=D)
     o = bi.sdpa(q.cuda(), k.cuda(), v.cuda(), causal=True, q_offset=0)
@@ -68,7 +71,7 @@ def test_single_visible_key_is_exact_head_dims(bi, D):
         assert torch.equal(o[0, h, 0].cpu(), v[0, 0, 0]), "head %d" % h
 
 
-@pytest.mark.parametrize("D", [64, 96])
+@pytest.mark.parametrize("D", [64, 96, 160, 224, 256])
 def test_columns_past_the_head_dim_untouched(bi, D):
     """The output is written for d < D only: a wider buffer keeps its other columns."""
     B, H, Hkv, Lq, Lkv = 1, 4, 2, 20, 300
@@ -79,7 +82,7 @@ def test_columns_past_the_head_dim_untouched(bi, D):
     assert_same_bits(wide[..., :D], bi.sdpa(q, k, v, causal=True), "strided out D=%d" % D)
 
 
-@pytest.mark.parametrize("D", [64, 96])
+@pytest.mark.parametrize("D", [64, 96, 256])
 @pytest.mark.parametrize("L0", [4095, 4097])
 def test_decode_equals_prefill_bits_head_dims(bi, D, L0):
     """C3's rule at the other head dims: a token's bits are the same in a 64-token prefill,
@@ -96,3 +99,31 @@ def test_decode_equals_prefill_bits_head_dims(bi, D, L0):
         assert_same_bits(pre[:, :, t:t + 1], more, "D=%d appended keys t=%d" % (D, t))
     one_b = bi.sdpa(q[1:2], k[1:2, :, :Lkv], v[1:2, :, :Lkv], causal=True, q_offset=L0)
     assert_same_bits(pre[1:2], one_b, "D=%d B=2 vs B=1" % D)
+
+
+def test_d256_graph_capture_and_long_decode(bi):
+    """256-column kernel: graph replay gives the eager bits; a longer decode (8192 keys,
+    sliding window + sinks) matches the oracle."""
+    B, H, Hkv, Lkv, D = 2, 8, 2, 8192, 256
+    q, k, v = synth.sdpa_qkv(B, H, Hkv, 1, Lkv, D, "bf16", seed=77)
+    pos = torch.arange(Lkv)
+    m = ((pos <= Lkv - 1) & (pos > Lkv - 1 - 3000)).view(1, Lkv)
+    sk = synth.normal((H,), 78, 2.0, "f32")
+    qc, kc, vc, mc, skc = q.cuda(), k.cuda(), v.cuda(), m.cuda(), sk.cuda()
+    eager = bi.sdpa(qc, kc, vc, mask=mc, sinks=skc)
+    ref, nrm = oracle.sdpa_ex(q, k, v, mask=m, sinks=sk)
+    check_close(eager, ref, nrm, torch.bfloat16, "D=256 decode window + sinks")
+    out = torch.empty_like(eager)
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(st):
+        bi.sdpa(qc, kc, vc, mask=mc, sinks=skc, out=out)
+    torch.cuda.current_stream().wait_stream(st)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        bi.sdpa(qc, kc, vc, mask=mc, sinks=skc, out=out)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert_same_bits(eager, out, "D=256 graph vs eager")
+    _no_device_error(bi)
