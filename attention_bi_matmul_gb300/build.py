@@ -20,7 +20,7 @@ OBJDIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libbi.so")
 
 SOURCES = ["api.cu", "gemm_f32.cu", "gemm_tc_bf16.cu", "gemm_tc_f16.cu", "sdpa.cu", "glue.cu",
-           "qgemm.cu", "sdpa256.cu"]
+           "qgemm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE]
 

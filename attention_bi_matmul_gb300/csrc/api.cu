@@ -120,7 +120,6 @@ bi_status device_init(int dev) {
     if ((st = init_gemm_tc_f16()) != BI_OK) return st;
     if ((st = init_sdpa()) != BI_OK) return st;
     if ((st = init_qgemm()) != BI_OK) return st;
-    if ((st = init_sdpa256()) != BI_OK) return st;
     if (!device_error_word()) return BI_ERR_CUDA;
     device_sm_count();
     if (!load_encode()) return BI_ERR_CUDA;
@@ -411,6 +410,7 @@ bi_status bi_sdpa_ex(const void *q, const int64_t qs[4], const void *k, const in
     a.qt = static_cast<int>(128 / G);
     a.D = static_cast<int>(D);
     a.dp = D <= 64 ? 64 : D <= 128 ? 128 : 256;
+    a.chunk = a.dp == 256 ? 64 : 128;
     a.mode = mask == BI_MASK_CAUSAL ? 1 : mask == BI_MASK_ARRAY ? 2 : 0;
     const double sc = scale > 0.0f ? static_cast<double>(scale) : 1.0 / std::sqrt(static_cast<double>(D));
     a.scale_log2 = static_cast<float>(sc * 1.4426950408889634);   // scale * log2(e)
@@ -437,7 +437,7 @@ bi_status bi_sdpa_ex(const void *q, const int64_t qs[4], const void *k, const in
         const uint64_t dims[4] = {static_cast<uint64_t>(D), static_cast<uint64_t>(Lkv),
                                   static_cast<uint64_t>(Hkv), static_cast<uint64_t>(B)};
         // key chunks of 128 (head dims up to 128) or 64 (the 256-column kernel)
-        const uint32_t box[4] = {64, a.dp == 256 ? 64u : 128u, 1, 1};
+        const uint32_t box[4] = {64, static_cast<uint32_t>(a.chunk), 1, 1};
         const uint64_t sk[3] = {static_cast<uint64_t>(ks[2]) * 2, static_cast<uint64_t>(ks[1]) * 2,
                                 static_cast<uint64_t>(ks[0]) * 2};
         st = encode_tmap(&tk, dtype, 4, const_cast<void *>(k), dims, sk, box, true);

@@ -54,7 +54,6 @@ bi_status init_gemm_tc_bf16();
 bi_status init_gemm_tc_f16();
 bi_status init_sdpa();
 bi_status init_qgemm();
-bi_status init_sdpa256();
 
 // ---- launchers
 bi_status launch_gemm_f32(const float *a, int64_t lda, const float *b, int64_t ldb, bool b_nk,
@@ -84,6 +83,7 @@ struct SdpaArgs {
     int qt;            // query positions per tile = 128 / group
     int D;             // head dim (64, 96, 128, 160, 192, 224 or 256)
     int dp;            // padded head dim of the kernel: 64, 128 or 256
+    int chunk;         // keys per chunk: 128 up to head dim 128, 64 above
     int mode;          // 0: no mask, 1: causal, 2: boolean array mask
     float scale_log2;  // scale * log2(e)
     void *o;
@@ -95,8 +95,6 @@ struct SdpaArgs {
 };
 bi_status launch_sdpa(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                       const SdpaArgs &args, bi_dtype dt, cudaStream_t s);
-bi_status launch_sdpa256(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                         const SdpaArgs &args, bi_dtype dt, cudaStream_t s);
 
 bi_status launch_rmsnorm(const void *x, int64_t ldx, const void *w, void *y, int64_t ldy,
                          int64_t M, int64_t N, float eps, bi_dtype dt, cudaStream_t s);
