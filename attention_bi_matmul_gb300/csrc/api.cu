@@ -199,14 +199,20 @@ bi_status encode_tmap_u32(CUtensorMap *map, int rank, void *base, const uint64_t
     return r == CUDA_SUCCESS ? BI_OK : BI_ERR_INVALID_ARG;
 }
 
-// Tile width of the tensor-core GEMM for (N, K, dtype, layout).  M is not an
+// Tile form of the tensor-core GEMM for (N, K, dtype, layout).  M is not an
 // input, and neither is anything else about the call.  Measured on GB300
-// (bf16, weights streamed from HBM): at K = 4096 a 128-column tile is within a
-// few percent of the best width for every M from 1 to 512 (it keeps N/128
-// blocks streaming weights for decode-shaped calls), while at K = 8192 the
-// 256-column tile is best both for decode-shaped calls and at M = 8192
-// (1.6 PFLOP/s vs 1.1 for 128 columns).  Hence: 256 columns from K = 8192 up,
-// 128 below.  Both widths exist for both weight layouts.
+// (bf16, weights streamed from HBM):
+//   * K = 4096: a 128 x 128 tile on one CTA is within a few percent of the best
+//     width for every M from 1 to 512 (it keeps N/128 blocks streaming weights
+//     for decode-shaped calls).  The 256 x 256 pair tile is slower there: each
+//     SM then runs the K loop of a 128 x 256 output, 25 us instead of 20.5 us
+//     at N = 11008, M = 1, and 614 us instead of 589 us over the M = 1..512 sweep.
+//   * K = 8192: 256 columns win both for decode-shaped calls and at M = 8192,
+//     and on a CTA pair (256 x 256, a third fewer bytes into each SM) the 8192^3
+//     product runs at 1.81 PFLOP/s, against 1.67 for 128 x 256 on one CTA and
+//     1.1 for 128 x 128.
+// Hence: 256 x 256 pair tiles from K = 8192 up, 128 x 128 below, for both
+// weight layouts.
 TcConfig tc_config(int64_t N, int64_t K, bi_dtype dt, bool b_mn_major) {
     (void)N;
     (void)dt;
@@ -214,6 +220,7 @@ TcConfig tc_config(int64_t N, int64_t K, bi_dtype dt, bool b_mn_major) {
     TcConfig c;
     c.block_n = K >= 8192 ? 256 : 128;
     c.stages = c.block_n == 256 ? 4 : 3;    // ring depth (stages of 1 or 2 K panels)
+    c.pair = c.block_n == 256;
     return c;
 }
 

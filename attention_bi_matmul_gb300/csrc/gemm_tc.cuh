@@ -7,8 +7,9 @@
 // no atomics, fp32 accumulators, bias added into the accumulator and rounded
 // once.  The GB300 form of that rule:
 //
-//   * output tile 128 x BN (BN chosen from (dtype, N, K, layout) only), one
-//     tcgen05.mma accumulator in tensor memory per tile;
+//   * output tile 128 x 128 on one CTA, or 256 x 256 on a CTA pair (the form
+//     chosen from (dtype, N, K, layout) only), one tcgen05.mma accumulator in
+//     tensor memory per tile;
 //   * K visited in ascending 64-wide blocks, each as four K=16 MMAs in
 //     ascending order, always starting from a zero accumulator -- for every M;
 //   * operands staged by TMA into a multi-stage shared-memory ring with
@@ -114,10 +115,11 @@ __host__ __device__ constexpr uint32_t tc_tmem_cols(int bn) {
            : (2 * bn <= 256) ? 256u : 512u;
 }
 
-// Pipeline shape per tile width, 192 KB of shared memory in both cases (with
-// 128-row A panels; fewer A rows leave room for more stages, see the kernel):
-//   128 columns: stages of 2 K panels (8 MMAs of 64 cycles per barrier round trip), 3 stages;
-//   256 columns: stages of 1 K panel (4 MMAs of 128 cycles), 4 stages.
+// Pipeline shape of the one-CTA kernel, 192 KB of shared memory (with 128-row A
+// panels; fewer A rows leave room for more stages, see the kernel): stages of 2
+// K panels (8 MMAs of 64 cycles per barrier round trip), 3 stages at 128
+// columns; stages of 1 K panel (4 MMAs of 128 cycles), 4 stages, at 256.  The
+// library builds the 128-column form; 256-column tiles run on a CTA pair below.
 template <int BN> __host__ __device__ constexpr int tc_kp() { return BN <= 128 ? 2 : 1; }
 template <int BN> __host__ __device__ constexpr int tc_stages() { return BN <= 128 ? 3 : 4; }
 template <int BN> __host__ __device__ constexpr bool tc_l2_prefetch() { return BN <= 128; }
@@ -356,6 +358,219 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (threadIdx.x == 0 && *abort_flag) atomicOr(args.err, ERR_TIMEOUT);
 }
 
+// ------------------------------------------------------------------ CTA-pair form
+//
+// The same rule on a pair of SMs (a cluster of two CTAs, cta_group::2): the
+// output tile is 256 x BN, one accumulator split over the pair's tensor
+// memories (rows 0-127 in the even CTA, 128-255 in the odd one).  Each CTA
+// stages its own 128 A rows and one half (BN/2 rows) of the B tile; the even
+// CTA's MMA thread issues the 256 x BN x 16 MMAs, which read both CTAs' shared
+// memory.  Per SM that is a 128 x BN output from 128 x 64 A plus BN/2 x 64 B
+// bytes per K panel -- a third fewer bytes into each SM than the one-CTA tile of
+// the same width, which is what bounds the one-CTA kernel on large GEMMs.
+// K is still visited in ascending 64-wide panels of four K = 16 steps from a zero
+// accumulator, and the tile of a row depends on nothing but the row.
+//
+// Barriers: full[s] lives in the even CTA and collects both CTAs' copy bytes;
+// empty[s] and tfull[b] exist in both CTAs and are signalled together by a
+// multicast commit; tempty[b] lives in the even CTA and counts the epilogue
+// warps of both.
+constexpr int TC2_BM = 256;         // rows per pair tile (128 per CTA)
+constexpr int TC2_RING_STAGES = 6;  // ring depth with 128-row A panels
+
+template <int BN>
+__host__ __device__ constexpr uint32_t tc2_ring_bytes() {
+    return (uint32_t)TC2_RING_STAGES * (TC_BM * TC_BK * 2 + (BN / 2) * TC_BK * 2);
+}
+template <int BN>
+__host__ __device__ constexpr size_t tc2_smem_bytes() {
+    return 1024 + tc2_ring_bytes<BN>() + (2 * TC_MAX_STAGES + 5) * 8 + 16;
+}
+
+template <typename T, int BN, bool B_MN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
+    gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA,
+                    const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
+    constexpr int BH = BN / 2;                               // B rows per CTA
+    constexpr uint32_t B_BYTES = BH * TC_BK * 2;             // per stage (one K panel)
+    constexpr uint32_t TMEM_COLS = tc_tmem_cols(BN);
+    constexpr uint32_t IDESC = mma_idesc(IsBf16<T>::value, TC2_BM, BN, B_MN);
+    static_assert(BN == 128 || BN == 256, "pair tile width");
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    // A stages first (a_rows rows each), then the B stages; the MMA reads 128 A
+    // rows, and rows past a_rows only feed tile rows that are never stored.  Both
+    // CTAs lay the ring out identically, so one descriptor addresses both.
+    const uint32_t A_BYTES = static_cast<uint32_t>(args.a_rows) * TC_BK * 2;
+    const uint32_t ST_FIT = tc2_ring_bytes<BN>() / (A_BYTES + B_BYTES);
+    const int STAGES = static_cast<int>(ST_FIT < TC_MAX_STAGES ? ST_FIT : TC_MAX_STAGES);
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + STAGES * A_BYTES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + tc2_ring_bytes<BN>());
+    uint64_t *empty = full + TC_MAX_STAGES;
+    uint64_t *tfull = empty + TC_MAX_STAGES;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *mma_done = tempty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+
+    const int64_t M = args.M, N = args.N, K = args.K;
+    const int64_t num_m = (M + TC2_BM - 1) / TC2_BM;
+    const int64_t num_n = (N + BN - 1) / BN;
+    const int64_t total = args.batch * num_m * num_n;
+    const int KB = static_cast<int>((K + TC_BK - 1) / TC_BK);
+    const int64_t pair = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 8);
+        }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncwarp();
+    cluster_sync();     // both CTAs' barriers initialised and TMEM allocated
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer (both CTAs)
+            prefetch_tmap(&tmA);
+            prefetch_tmap(&tmB);
+            const uint32_t tx = 2u * (A_BYTES + B_BYTES);       // both CTAs' bytes
+            uint32_t it = 0, s = 0, ph = 0;
+            bool ok = true;
+            for (int64_t t = pair; ok && t < total; t += num_pairs) {
+                int64_t e, mb, nb;
+                tc_tile_coords(t, num_m, num_n, e, mb, nb);
+                const int32_t ea = args.sa ? static_cast<int32_t>(e) : 0;
+                const int32_t eb = args.sb ? static_cast<int32_t>(e) : 0;
+                const int32_t row0 = static_cast<int32_t>(mb * TC2_BM + rank * TC_BM);
+                const int32_t col0 = static_cast<int32_t>(nb * BN + rank * BH);
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
+                    const uint32_t fb = cluster_addr(&full[s], 0);
+                    if (leader) mbar_arrive_expect_tx(&full[s], tx);
+                    const int32_t k0 = kb * TC_BK;               // beyond K: zero-filled
+                    tma_load_3d_pair(sA + s * A_BYTES, &tmA, fb, k0, row0, ea);
+                    if (!B_MN) {
+                        tma_load_3d_pair(sB + s * B_BYTES, &tmB, fb, k0, col0, eb);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < BH / 64; ++j)
+                            tma_load_3d_pair(sB + s * B_BYTES + j * 8192, &tmB, fb, col0 + j * 64,
+                                             k0, eb);
+                    }
+                    if (++s == STAGES) { s = 0; ph ^= 1u; }
+                }
+            }
+            if (!ok) {
+                // Let the copies already issued land before the pair can exit.  The
+                // even CTA's barriers see both CTAs' bytes; the odd CTA cannot wait on
+                // them, so it gives its own copies a fixed time instead.
+                if (leader) {
+                    const uint32_t first = it > static_cast<uint32_t>(STAGES) ? it - STAGES : 0;
+                    for (uint32_t i = first; i < it; ++i)
+                        mbar_wait_limited(&full[i % STAGES], (i / STAGES) & 1u, WAIT_LIMIT_NS);
+                } else {
+                    const uint64_t t0 = globaltimer_ns();
+                    for (uint32_t i = 0; i < WAIT_MAX_ROUNDS && globaltimer_ns() - t0 < 1000000ull; ++i)
+                        __nanosleep(1000);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            // ------------------------------------------------ MMA issuer (even CTA)
+            const uint64_t a_desc0 = smem_desc(smem_u32(sA), 16, 1024);
+            const uint64_t b_desc0 = B_MN ? smem_desc(smem_u32(sB), 8192, 1024)
+                                          : smem_desc(smem_u32(sB), 16, 1024);
+            const uint64_t A_STEP = A_BYTES >> 4;
+            constexpr uint64_t B_STEP = B_BYTES >> 4;
+            constexpr uint64_t BK_STEP = B_MN ? (2048 >> 4) : (32 >> 4);
+            uint32_t tc = 0, s = 0, ph = 0;
+            bool ok = true;
+            for (int64_t t = pair; ok && t < total; t += num_pairs, ++tc) {
+                const uint32_t acc = tc & 1u;
+                const uint32_t aph = (tc >> 1) & 1u;
+                if (!mbar_wait_cluster(&tempty[acc], aph ^ 1u, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(&full[s], ph, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t ad = a_desc0 + s * A_STEP;
+                    const uint64_t bd = b_desc0 + s * B_STEP;
+#pragma unroll
+                    for (int j = 0; j < TC_BK / 16; ++j)
+                        mma_f16_ss_pair(d_tmem, ad + j * (32 >> 4), bd + j * BK_STEP, IDESC,
+                                        (kb | j) != 0 ? 1u : 0u);
+                    mma_commit_pair_mc(&empty[s], 0x3);
+                    if (++s == STAGES) { s = 0; ph ^= 1u; }
+                }
+                if (!ok) break;
+                mma_commit_pair_mc(&tfull[acc], 0x3);
+            }
+            // All issued MMAs must be complete before either CTA releases TMEM or
+            // shared memory.
+            mma_commit_pair(mma_done);
+            mbar_wait_limited(mma_done, 0, WAIT_LIMIT_NS);
+        }
+    } else if (warp >= 2 && warp <= 5) {
+        // ------------------------------------------------ epilogue (both CTAs)
+        const uint32_t quarter = static_cast<uint32_t>(warp & 3);
+        const int row_in_tile = static_cast<int>(rank) * TC_BM + static_cast<int>(quarter) * 32 + lane;
+        uint32_t tc = 0;
+        for (int64_t t = pair; t < total; t += num_pairs, ++tc) {
+            int64_t e, mb, nb;
+            tc_tile_coords(t, num_m, num_n, e, mb, nb);
+            const uint32_t acc = tc & 1u;
+            const uint32_t aph = (tc >> 1) & 1u;
+            if (!warp_wait(&tfull[acc], aph, abort_flag)) break;
+            tc_fence_after();
+            const int64_t m = mb * TC2_BM + row_in_tile;
+#pragma unroll 1
+            for (int cc = 0; cc < BN / 32; ++cc) {
+                uint32_t r[32];
+                tmem_ld32(tmem_base + ((quarter * 32u) << 16) + acc * BN + cc * 32, r);
+                tmem_wait_ld(r);
+                if (m < M) gemm_epilogue32<T>(r, e, m, nb * BN + cc * 32, args);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(cluster_addr(&tempty[acc], 0));
+        }
+    }
+
+    tc_fence_before();
+    __syncwarp();
+    cluster_sync();     // no MMA, copy or arrival is still headed for either CTA
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    }
+    if (threadIdx.x == 0 && *abort_flag) atomicOr(args.err, ERR_TIMEOUT);
+}
+
 // Host side: instantiate and launch one configuration.
 // Shared-memory attribute of one instantiation (per device; done at library init).
 template <typename T, int BN, bool B_MN>
@@ -365,13 +580,46 @@ bi_status init_tc_inst() {
                                             static_cast<int>(tc_smem_bytes<BN>())));
 }
 
+// Pair kernel: the shared-memory attribute and how many pairs fit on the device
+// at once (the persistent grid must never exceed it: a pair that is not resident
+// would only start once another has finished all its tiles).
+constexpr int TC2_MAX_DEVICES = 64;
+template <typename T, int BN, bool B_MN>
+int &tc2_max_pairs(int dev) {
+    static int v[TC2_MAX_DEVICES] = {};
+    return v[dev];
+}
+
+template <typename T, int BN, bool B_MN>
+bi_status init_tc2_inst() {
+    constexpr size_t SMEM = tc2_smem_bytes<BN>();
+    bi_status st = cuda_status(cudaFuncSetAttribute(gemm_tc2_kernel<T, BN, B_MN>,
+                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                    static_cast<int>(SMEM)));
+    if (st != BI_OK) return st;
+    int dev = 0;
+    if ((st = cuda_status(cudaGetDevice(&dev))) != BI_OK) return st;
+    if (dev < 0 || dev >= TC2_MAX_DEVICES) return BI_ERR_UNSUPPORTED;
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(2 * static_cast<unsigned>(device_sm_count()));
+    lc.blockDim = dim3(TC_THREADS);
+    lc.dynamicSmemBytes = SMEM;
+    int clusters = 0;
+    if ((st = cuda_status(cudaOccupancyMaxActiveClusters(&clusters, gemm_tc2_kernel<T, BN, B_MN>,
+                                                         &lc))) != BI_OK)
+        return st;
+    if (clusters <= 0) return BI_ERR_UNSUPPORTED;
+    tc2_max_pairs<T, BN, B_MN>(dev) = clusters;
+    return BI_OK;
+}
+
 template <typename T>
 bi_status init_tc_all() {
     bi_status st;
     if ((st = init_tc_inst<T, 128, false>()) != BI_OK) return st;
-    if ((st = init_tc_inst<T, 256, false>()) != BI_OK) return st;
     if ((st = init_tc_inst<T, 128, true>()) != BI_OK) return st;
-    return init_tc_inst<T, 256, true>();
+    if ((st = init_tc2_inst<T, 256, false>()) != BI_OK) return st;
+    return init_tc2_inst<T, 256, true>();
 }
 
 template <typename T, int BN, bool B_MN>
@@ -388,6 +636,23 @@ bi_status launch_tc_inst(const CUtensorMap &ta, const CUtensorMap &tb, const Gem
     return cuda_status(cudaGetLastError());
 }
 
+template <typename T, int BN, bool B_MN>
+bi_status launch_tc2_inst(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &args,
+                          cudaStream_t s) {
+    constexpr size_t SMEM = tc2_smem_bytes<BN>();
+    const int64_t tiles =
+        args.batch * ((args.M + TC2_BM - 1) / TC2_BM) * ((args.N + BN - 1) / BN);
+    int dev = 0;
+    bi_status st = cuda_status(cudaGetDevice(&dev));
+    if (st != BI_OK) return st;
+    if (dev < 0 || dev >= TC2_MAX_DEVICES) return BI_ERR_UNSUPPORTED;
+    const int max_pairs = tc2_max_pairs<T, BN, B_MN>(dev);
+    if (max_pairs <= 0) return BI_ERR_CUDA;    // not initialised on this device
+    const int pairs = static_cast<int>(tiles < max_pairs ? tiles : max_pairs);
+    gemm_tc2_kernel<T, BN, B_MN><<<2 * pairs, TC_THREADS, SMEM, s>>>(ta, tb, args);
+    count_launch();
+    return cuda_status(cudaGetLastError());
+}
 
 // Dispatch on the configured tile width; builds the tensor maps.
 template <typename T>
@@ -413,25 +678,22 @@ bi_status launch_gemm_tc_typed(const void *a, int64_t lda, const void *b, int64_
         const uint64_t dims[3] = {inner, outer, eb};
         const uint64_t strides[2] = {static_cast<uint64_t>(ldb) * 2,
                                      static_cast<uint64_t>(args.sb ? args.sb : ldb * outer) * 2};
+        // K-major B: one box of the tile's rows (half of them per CTA in the pair
+        // form); MN-major B: 64-column boxes.
+        const uint32_t b_rows = static_cast<uint32_t>(cfg.pair ? BN / 2 : BN);
         const uint32_t box[3] = {b_nk ? static_cast<uint32_t>(TC_BK) : 64u,
-                                 b_nk ? static_cast<uint32_t>(BN) : static_cast<uint32_t>(TC_BK),
-                                 1};
+                                 b_nk ? b_rows : static_cast<uint32_t>(TC_BK), 1};
         bi_status st = encode_tmap(&tb, dt, 3, const_cast<void *>(b), dims, strides, box, true);
         if (st != BI_OK) return st;
     }
-    if (b_nk) {
-        switch (BN) {
-            case 128: return launch_tc_inst<T, 128, false>(ta, tb, args, cfg.stages, s);
-            case 256: return launch_tc_inst<T, 256, false>(ta, tb, args, cfg.stages, s);
-            default: return BI_ERR_UNSUPPORTED;
-        }
-    } else {
-        switch (BN) {
-            case 128: return launch_tc_inst<T, 128, true>(ta, tb, args, cfg.stages, s);
-            case 256: return launch_tc_inst<T, 256, true>(ta, tb, args, cfg.stages, s);
-            default: return BI_ERR_UNSUPPORTED;
-        }
-    }
+    // Built forms: 128-column tiles on one CTA, 256-column tiles on a CTA pair.
+    if (cfg.pair && BN == 256)
+        return b_nk ? launch_tc2_inst<T, 256, false>(ta, tb, args, s)
+                    : launch_tc2_inst<T, 256, true>(ta, tb, args, s);
+    if (!cfg.pair && BN == 128)
+        return b_nk ? launch_tc_inst<T, 128, false>(ta, tb, args, cfg.stages, s)
+                    : launch_tc_inst<T, 128, true>(ta, tb, args, cfg.stages, s);
+    return BI_ERR_UNSUPPORTED;
 }
 
 }  // namespace bi

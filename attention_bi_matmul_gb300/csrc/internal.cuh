@@ -35,6 +35,7 @@ struct GemmArgs {
 struct TcConfig {
     int block_n;
     int stages;
+    bool pair;      // 256-row tiles on a CTA pair (cta_group::2)
 };
 
 // ---- host helpers (api.cu)

@@ -502,7 +502,7 @@ def run_ours(args):
     if dom == "gemm_8192":
         roof = {"bound": "tensor", "achieved": pinfo[dom]["tflops"], "peak": tf_burst,
                 "unit": "TFLOP/s", "frac": round(pinfo[dom]["tflops"] / tf_burst, 4),
-                "traffic": traffic, "kernel": "gemm_tc_kernel (bi_linear 8192^3)",
+                "traffic": traffic, "kernel": "gemm_tc2_kernel (bi_linear 8192^3, CTA pairs)",
                 "peak_source": peak_src + " bf16 burst"}
     else:
         roof = {"bound": "hbm", "achieved": pinfo[dom]["gbs"], "peak": hbm, "unit": "GB/s",

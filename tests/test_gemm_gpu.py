@@ -238,3 +238,58 @@ def test_repeated_runs_identical(bi):
     y0 = bi.matmul(a, b)
     for _ in range(3):
         assert_same_bits(bi.matmul(a, b), y0, "repeat")
+
+
+# ------------------------------------------------------------------ the CTA-pair tile (K >= 8192)
+
+@pytest.mark.parametrize("dt", ["bf16", "fp16"])
+def test_pair_tile_linear_rows_invariant(bi, dt):
+    """K-major weights on the 256-row pair tile: a row's bits do not depend on M, across
+    the 128-row boundary between the pair's CTAs and the 256-row boundary between tiles."""
+    K, N = 8192, 1000
+    x, w = synth.gemm16(700, N, K, dt, seed=31, layout="linear", device="cuda")
+    full = bi.linear(x, w)
+    for M in (1, 16, 127, 128, 129, 255, 256, 257, 511, 512, 700):
+        assert_same_bits(bi.linear(x[:M], w), full[:M], "linear K=8192 M=%d" % M)
+    rows = [0, 127, 128, 255, 256, 383, 384, 699]
+    cols = np.r_[0:70, 930:1000]
+    ref, nrm = oracle.linear(x[rows].cpu(), w[cols].cpu())
+    check_close(full[rows][:, cols], ref, nrm, DT[dt], "pair linear sampled")
+    _no_device_error(bi)
+
+
+@pytest.mark.parametrize("layout", ["linear", "matmul"])
+def test_pair_tile_more_tiles_than_pairs(bi, layout):
+    """2304 x 2600 outputs at K = 8192: 9 x 11 = 99 pair tiles, more than the pairs the
+    device holds at once, so pairs loop over tiles and both accumulator buffers turn over."""
+    M, N, K = 2304, 2600, 8192
+    a, b = synth.gemm16(M, N, K, "bf16", seed=32, layout=layout, device="cuda")
+    y = bi.linear(a, b) if layout == "linear" else bi.matmul(a, b)
+    rows = [0, 255, 256, 1151, 2047, 2303]
+    cols = np.r_[0:40, 1280:1300, 2560:2600]
+    if layout == "linear":
+        ref, nrm = oracle.linear(a[rows].cpu(), b[cols].cpu())
+    else:
+        ref, nrm = oracle.matmul(a[rows].cpu(), b[:, cols].contiguous().cpu())
+    check_close(y[rows][:, cols], ref, nrm, torch.bfloat16, "pair %s 2304x2600" % layout)
+    # the first 300 rows alone give the same bits
+    y2 = bi.linear(a[:300], b) if layout == "linear" else bi.matmul(a[:300], b)
+    assert_same_bits(y2, y[:300], "pair %s first 300 rows" % layout)
+    _no_device_error(bi)
+
+
+def test_pair_tile_batched_entries(bi):
+    """Batched matmul at K = 8192 (pair tiles with a batch coordinate): each entry equals
+    its own unbatched product, bit for bit, for a shared and a per-entry right operand."""
+    Bt, M, N, K = 3, 200, 264, 8192
+    g = torch.Generator().manual_seed(33)
+    a = (torch.randn(Bt, M, K, generator=g) / 64).to(torch.bfloat16).cuda()
+    b = (torch.randn(Bt, K, N, generator=g) / 64).to(torch.bfloat16).cuda()
+    y = bi.bmm(a, b)
+    ys = bi.bmm(a, b[0])
+    for e in range(Bt):
+        assert_same_bits(y[e], bi.matmul(a[e], b[e]), "entry %d" % e)
+        assert_same_bits(ys[e], bi.matmul(a[e], b[0]), "shared b entry %d" % e)
+    ref, nrm = oracle.matmul(a[1, :9].cpu(), b[1].cpu())
+    check_close(y[1, :9], ref, nrm, torch.bfloat16, "pair bmm entry 1")
+    _no_device_error(bi)
