@@ -17,8 +17,11 @@
 //     in ascending order, C = 128 for head dims up to 128 and 64 above (a
 //     function of the head dim alone).  For each chunk: S = Q K^T
 //     (tcgen05.mma into tensor memory); the mask (causal: key j visible iff
-//     j <= position; none; or a boolean array); m' = max(m, (max of the
-//     visible s_j) * c) with c = scale * log2 e; alpha = 2^(m - m');
+//     j <= position; none; or a boolean array); with c = scale * log2 e and
+//     x = (max of the visible s_j) * c, the row's shift m moves to m' = x only
+//     if x > m + 8, and otherwise stays (m' = m): the shift may lag the
+//     running maximum by up to 8, so p <= 2^8, and most chunks leave it and
+//     the accumulator alone; alpha = 2^(m - m') (exactly 1 when m' = m);
 //     p_j = 2^(fma(s_j, c, -m')); l = l * alpha + (half sum + half sum), each
 //     half summed as four interleaved partial sums (key mod 4) added as
 //     (0+1)+(2+3); P rounded to the input dtype;
@@ -68,6 +71,7 @@ constexpr int S2_KST = 2;          // K ring depth
 constexpr int S2_VST = 2;          // V ring depth
 constexpr int S2_THREADS = 320;
 constexpr uint32_t S2_QPANEL = S2_ROWS * 128;     // 16 KB: 128 rows x 64 elements
+constexpr float S2_LAG = 8.0f;     // how far a row's shift may lag its running maximum (log2)
 
 // DP: padded head dim (64, 128, 256); C: keys per chunk (64 or 128).
 template <int DP, int C>
@@ -318,7 +322,7 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
                 }
                 if (full) {
 #pragma unroll
-                    for (int i = 0; i < HK; ++i) mloc = fmaxf(mloc, x[i]);
+                    for (int i = 0; i < HK; i += 2) mloc = fmax3(mloc, x[i], x[i + 1]);
                 } else {
 #pragma unroll
                     for (int i = 0; i < HK; ++i)
@@ -332,19 +336,31 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
             pair_sync(quarter);
             const float mraw = fmaxf(mx_s[r], mx_s[128 + r]);
             const bool any = mraw != -INFINITY;
-            const float m_new = any ? fmaxf(m_run, __fmul_rn(mraw, sl2)) : m_run;
-            const float alpha = any ? ex2_approx(__fsub_rn(m_run, m_new)) : 1.0f;
-            float ls4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            const float cand = __fmul_rn(mraw, sl2);
+            const bool raise = any && cand > __fadd_rn(m_run, S2_LAG);
+            const float m_new = raise ? cand : m_run;
+            const float alpha = raise ? ex2_approx(__fsub_rn(m_run, m_new)) : 1.0f;
+            // Keys in pairs with the packed fp32 forms (each lane rounds as the scalar
+            // operation does): partial sum (key mod 4) k lives in ls01 (k = 0, 1) or
+            // ls23 (k = 2, 3) and is added in ascending key order.
+            float2 ls01 = make_float2(0.0f, 0.0f), ls23 = make_float2(0.0f, 0.0f);
             if (warp_valid) {
+                const float2 c2 = make_float2(sl2, sl2), nm2 = make_float2(-m_new, -m_new);
 #pragma unroll
-                for (int i = 0; i < HK; ++i) {
-                    float e = ex2_approx(__fmaf_rn(x[i], sl2, -m_new));
-                    if (!full && (ARR ? ((vis >> i) & 1u) == 0 : i >= lim)) e = 0.0f;
-                    x[i] = e;
-                    ls4[i & 3] = __fadd_rn(ls4[i & 3], e);
+                for (int i = 0; i < HK; i += 2) {
+                    const float2 t = __ffma2_rn(make_float2(x[i], x[i + 1]), c2, nm2);
+                    float e0 = ex2_approx(t.x), e1 = ex2_approx(t.y);
+                    if (!full) {
+                        if (ARR ? ((vis >> i) & 1u) == 0 : i >= lim) e0 = 0.0f;
+                        if (ARR ? ((vis >> (i + 1)) & 1u) == 0 : i + 1 >= lim) e1 = 0.0f;
+                    }
+                    x[i] = e0;
+                    x[i + 1] = e1;
+                    if ((i & 2) == 0) ls01 = __fadd2_rn(ls01, make_float2(e0, e1));
+                    else ls23 = __fadd2_rn(ls23, make_float2(e0, e1));
                 }
             }
-            const float lsum = __fadd_rn(__fadd_rn(ls4[0], ls4[1]), __fadd_rn(ls4[2], ls4[3]));
+            const float lsum = __fadd_rn(__fadd_rn(ls01.x, ls01.y), __fadd_rn(ls23.x, ls23.y));
             // P_j and the rescaled O must wait until P_{j-1} V_{j-1} is added in
             if (j >= 1) {
                 warp_wait(pvdone, (j - 1) & 1u, abort_flag);

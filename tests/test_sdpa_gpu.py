@@ -166,3 +166,30 @@ def test_decode_full_size_sampled(bi):
         ref, nrm = oracle.sdpa(q[b:b + 1].cpu(), k[b:b + 1].cpu(), v[b:b + 1].cpu(), causal=True)
         check_close(o[b:b + 1], ref, nrm, torch.bfloat16, "decode b=%d" % b)
     _no_device_error(bi)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "fp16"])
+def test_growing_scores_move_the_shift(bi, dt):
+    """Keys whose scale grows along the sequence, so a row's chunk maxima keep rising far
+    past its shift (the shift must move many times, by more than 2^8 each): parity with
+    the oracle, and a token's bits are the same alone (decode), inside a 256-row chunk
+    and inside the whole prefill."""
+    B, H, Hkv, L, D = 1, 8, 2, 1024, 128
+    g = torch.Generator().manual_seed(41)
+    q = torch.randn(B, H, L, D, generator=g)
+    grow = (1.0 + torch.arange(L, dtype=torch.float32) / 32.0).view(1, 1, L, 1)
+    k = torch.randn(B, Hkv, L, D, generator=g) * grow
+    v = torch.randn(B, Hkv, L, D, generator=g)
+    q, k, v = (t.to(DT[dt]) for t in (q, k, v))
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o = bi.sdpa(qd, kd, vd, causal=True)
+    for p in (0, 1, 127, 128, 500, 1000, 1023):
+        # row p sees keys 0..p: the oracle on that prefix with q_offset = p
+        ref, nrm = oracle.sdpa(q[:, :, p:p + 1], k[:, :, :p + 1], v[:, :, :p + 1], causal=True)
+        check_close(o[:, :, p:p + 1], ref, nrm, DT[dt], "growing scores, row %d" % p)
+    for p in (700, 1023):
+        one = bi.sdpa(qd[:, :, p:p + 1], kd[:, :, :p + 1], vd[:, :, :p + 1], causal=True)
+        assert_same_bits(one, o[:, :, p:p + 1], "token %d alone vs in the prefill" % p)
+        tile = bi.sdpa(qd[:, :, p - 255:p + 1], kd[:, :, :p + 1], vd[:, :, :p + 1], causal=True)
+        assert_same_bits(tile[:, :, -1:], o[:, :, p:p + 1], "token %d in a 256-row chunk" % p)
+    _no_device_error(bi)
