@@ -47,7 +47,9 @@
 // Roles (320 threads):
 //   warp 0 lane 0   TMA producer (Q once; K and V chunks through 2-deep rings)
 //   warp 1          TMEM allocation (S0, S1 of C columns, O of DP); lane 0
-//                   issues the MMAs
+//                   issues the MMAs, waiting twice per chunk (K_j with V_{j-1},
+//                   then P_{j-1}): every barrier wait of the issuing thread leaves
+//                   the tensor pipe idle for a few hundred cycles
 //   warps 2..9      row warps: warp w serves TMEM lane quarter w % 4 and half
 //                   (w-2)/4 of the keys (C/2) and of the output columns (DP/2);
 //                   the two warps of a row exchange the chunk maximum and the
@@ -88,8 +90,8 @@ struct S2Smem {
     static constexpr uint32_t MX = P + PB;                       // float[2][128] half maxima
     static constexpr uint32_t LS = MX + 2 * 128 * 4;             // float[2][128] half sums
     static constexpr uint32_t BARS = LS + 2 * 128 * 4;
-    // bar_q kfull[2] kempty[2] vfull[2] vempty[2] sfull[2] sempty[2] pfull pvdone mma_done
-    static constexpr uint32_t NBARS = 1 + 2 * S2_KST + 2 * S2_VST + 4 + 3;
+    // bar_q kvfull[2] kempty[2] vempty[2] sfull[2] pfull pvdone mma_done
+    static constexpr uint32_t NBARS = 1 + 2 + S2_KST + S2_VST + 2 + 3;
     static constexpr uint32_t MISC = BARS + NBARS * 8;           // tmem slot, abort flag
     static constexpr uint32_t END = MISC + 16;
     static constexpr size_t BYTES = 1024 + END;
@@ -125,13 +127,11 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
     float *ls_s = reinterpret_cast<float *>(smem + S2Smem::LS);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S2Smem::BARS);
     uint64_t *bar_q = bars;
-    uint64_t *kfull = bar_q + 1;
-    uint64_t *kempty = kfull + S2_KST;
-    uint64_t *vfull = kempty + S2_KST;
-    uint64_t *vempty = vfull + S2_VST;
+    uint64_t *kvfull = bar_q + 1;        // [2] step j: K_j and V_{j-1} have landed
+    uint64_t *kempty = kvfull + 2;
+    uint64_t *vempty = kempty + S2_KST;
     uint64_t *sfull = vempty + S2_VST;   // [2]
-    uint64_t *sempty = sfull + 2;        // [2]
-    uint64_t *pfull = sempty + 2;        // P_j in smem and O rescaled for chunk j
+    uint64_t *pfull = sfull + 2;         // P_j in smem and O rescaled for chunk j
     uint64_t *pvdone = pfull + 1;        // P_j V_j added into O (P free, O readable)
     uint64_t *mma_done = pvdone + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S2Smem::MISC);
@@ -157,11 +157,11 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(bar_q, 1);
-        for (int s = 0; s < S2_KST; ++s) { mbar_init(&kfull[s], 1); mbar_init(&kempty[s], 1); }
-        for (int s = 0; s < S2_VST; ++s) { mbar_init(&vfull[s], 1); mbar_init(&vempty[s], 1); }
+        for (int s = 0; s < 2; ++s) mbar_init(&kvfull[s], 1);
+        for (int s = 0; s < S2_KST; ++s) mbar_init(&kempty[s], 1);
+        for (int s = 0; s < S2_VST; ++s) mbar_init(&vempty[s], 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sfull[i], 1);
-            mbar_init(&sempty[i], 8);
         }
         mbar_init(pfull, 8);
         mbar_init(pvdone, 1);
@@ -189,33 +189,45 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
 #pragma unroll
             for (uint32_t pn = 0; pn < NP; ++pn)
                 tma_load_4d(sQ + pn * S2_QPANEL, &tmQ, bar_q, 64 * pn, kvh * G, qi0, b);
+            // Step j loads K_j and V_{j-1} onto one barrier, so that the MMA thread
+            // waits once per chunk for both (each wait costs the tensor pipe time).
+            // Every step, the last one (V only) included, first waits for the K slot
+            // release of step j-2 (S(j-2) done): the MMA thread issues S(j-2) only
+            // after its wait on step j-2, which used this same barrier, so the barrier
+            // is never armed again before that phase has been consumed.
             int armed = 0;
             bool ok = true;
-            for (int j = 0; j < nchunks; ++j) {
-                const uint32_t sk = j % S2_KST, phk = (j / S2_KST) & 1u;
-                if (!mbar_wait(&kempty[sk], phk ^ 1u, abort_flag)) { ok = false; break; }
-                mbar_arrive_expect_tx(&kfull[sk], S2_KV);
+            for (int j = 0; j <= nchunks; ++j) {
+                const bool has_k = j < nchunks, has_v = j >= 1;
+                if (!mbar_wait(&kempty[j % S2_KST], ((j / S2_KST) & 1u) ^ 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (has_v && !mbar_wait(&vempty[(j - 1) % S2_VST], (((j - 1) / S2_VST) & 1u) ^ 1u,
+                                        abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&kvfull[j & 1], (has_k ? S2_KV : 0u) + (has_v ? S2_KV : 0u));
+                if (has_k) {
 #pragma unroll
-                for (uint32_t pn = 0; pn < NP; ++pn)
-                    tma_load_4d(sK + sk * S2_KV + pn * S2_KPANEL, &tmK, &kfull[sk], 64 * pn,
-                                j * S2_C, kvh, b);
-                const uint32_t sv = j % S2_VST, phv = (j / S2_VST) & 1u;
-                if (!mbar_wait(&vempty[sv], phv ^ 1u, abort_flag)) { ok = false; armed = 2 * j + 1; break; }
-                mbar_arrive_expect_tx(&vfull[sv], S2_KV);
+                    for (uint32_t pn = 0; pn < NP; ++pn)
+                        tma_load_4d(sK + (j % S2_KST) * S2_KV + pn * S2_KPANEL, &tmK, &kvfull[j & 1],
+                                    64 * pn, j * S2_C, kvh, b);
+                }
+                if (has_v) {
 #pragma unroll
-                for (uint32_t pn = 0; pn < NP; ++pn)
-                    tma_load_4d(sV + sv * S2_KV + pn * S2_KPANEL, &tmV, &vfull[sv], 64 * pn,
-                                j * S2_C, kvh, b);
-                armed = 2 * j + 2;
+                    for (uint32_t pn = 0; pn < NP; ++pn)
+                        tma_load_4d(sV + ((j - 1) % S2_VST) * S2_KV + pn * S2_KPANEL, &tmV,
+                                    &kvfull[j & 1], 64 * pn, (j - 1) * S2_C, kvh, b);
+                }
+                armed = j + 1;
             }
             if (!ok) {
                 // Let every copy already issued land before the block can exit.
                 mbar_wait_limited(bar_q, 0, WAIT_LIMIT_NS);
-                const int nk = (armed + 1) / 2, nv = armed / 2;
-                for (int j = nk - S2_KST < 0 ? 0 : nk - S2_KST; j < nk; ++j)
-                    mbar_wait_limited(&kfull[j % S2_KST], (j / S2_KST) & 1u, WAIT_LIMIT_NS);
-                for (int j = nv - S2_VST < 0 ? 0 : nv - S2_VST; j < nv; ++j)
-                    mbar_wait_limited(&vfull[j % S2_VST], (j / S2_VST) & 1u, WAIT_LIMIT_NS);
+                for (int j = armed - 2 < 0 ? 0 : armed - 2; j < armed; ++j)
+                    mbar_wait_limited(&kvfull[j & 1], (j >> 1) & 1u, WAIT_LIMIT_NS);
             }
         }
     } else if (warp == 1) {
@@ -225,13 +237,15 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
             const uint32_t q_addr = smem_u32(sQ);
             const uint32_t p_addr = smem_u32(sP);
             for (int j = 0; ok && j <= nchunks; ++j) {
+                // step j: K_j (if j < nchunks) and V_{j-1} (if j >= 1) have landed
+                if (!mbar_wait(&kvfull[j & 1], (j >> 1) & 1u, abort_flag)) { ok = false; break; }
+                tc_fence_after();
                 if (j < nchunks) {
-                    // S(j) = Q K_j^T into S buffer j & 1 (DP / 16 steps over the head dim)
+                    // S(j) = Q K_j^T into S buffer j & 1 (DP / 16 steps over the head dim).
+                    // That buffer held S(j-2), which the row warps read before writing
+                    // P(j-2), whose barrier this thread waited for at step j-1.
                     const uint32_t sk = j % S2_KST;
                     const uint32_t sb = j & 1;
-                    if (!mbar_wait(&kfull[sk], (j / S2_KST) & 1u, abort_flag)) { ok = false; break; }
-                    if (!mbar_wait(&sempty[sb], ((j >> 1) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
-                    tc_fence_after();
                     const uint32_t k_addr = smem_u32(sK + sk * S2_KV);
 #pragma unroll
                     for (int kk = 0; kk < DP / 16; ++kk) {
@@ -248,7 +262,6 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
                     const int i = j - 1;
                     const uint32_t sv = i % S2_VST;
                     if (!mbar_wait(pfull, i & 1u, abort_flag)) { ok = false; break; }
-                    if (!mbar_wait(&vfull[sv], (i / S2_VST) & 1u, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t v_addr = smem_u32(sV + sv * S2_KV);
 #pragma unroll
@@ -329,9 +342,6 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
                         if (ARR ? ((vis >> i) & 1u) != 0 : i < lim) mloc = fmaxf(mloc, x[i]);
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sempty[sb]);
             mx_s[half * 128 + r] = mloc;
             pair_sync(quarter);
             const float mraw = fmaxf(mx_s[r], mx_s[128 + r]);

@@ -193,3 +193,19 @@ def test_growing_scores_move_the_shift(bi, dt):
         tile = bi.sdpa(qd[:, :, p - 255:p + 1], kd[:, :, :p + 1], vd[:, :, :p + 1], causal=True)
         assert_same_bits(tile[:, :, -1:], o[:, :, p:p + 1], "token %d in a 256-row chunk" % p)
     _no_device_error(bi)
+
+
+def test_two_chunk_decode_many_ctas_repeated(bi):
+    """Decode where every block sees exactly two key chunks (the last step of the key/value
+    pipeline then carries only values), with 256 blocks in flight and the call repeated:
+    every launch gives the same bits, and sampled rows match the oracle."""
+    B, H, Hkv, Lkv, D = 32, 32, 8, 200, 128
+    q, k, v = synth.sdpa_qkv(B, H, Hkv, 1, Lkv, D, "bf16", seed=51)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    first = bi.sdpa(qd, kd, vd, causal=True)
+    for _ in range(20):
+        assert_same_bits(bi.sdpa(qd, kd, vd, causal=True), first, "repeated two-chunk decode")
+    for b in (0, 17, 31):
+        ref, nrm = oracle.sdpa(q[b:b + 1], k[b:b + 1], v[b:b + 1], causal=True)
+        check_close(first[b:b + 1], ref, nrm, torch.bfloat16, "two-chunk decode b=%d" % b)
+    _no_device_error(bi)
