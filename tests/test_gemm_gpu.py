@@ -293,3 +293,24 @@ def test_pair_tile_batched_entries(bi):
     ref, nrm = oracle.matmul(a[1, :9].cpu(), b[1].cpu())
     check_close(y[1, :9], ref, nrm, torch.bfloat16, "pair bmm entry 1")
     _no_device_error(bi)
+
+
+@pytest.mark.parametrize("layout", ["linear", "matmul"])
+def test_pair_tile_stage_shape_keeps_bits(bi, layout):
+    """The pair kernel stages two K panels at a time when every pair has at least two tiles
+    (4096 x 2600 at K = 8192: 16 x 11 = 176 tiles) and one otherwise (the first 256 rows
+    alone: 11 tiles). The stage shape is scheduling only: the rows' bits must agree."""
+    M, N, K = 4096, 2600, 8192
+    a, b = synth.gemm16(M, N, K, "bf16", seed=34, layout=layout, device="cuda")
+    fn = bi.linear if layout == "linear" else bi.matmul
+    full = fn(a, b)
+    assert_same_bits(fn(a[:256], b), full[:256], "%s first 256 rows vs all 4096" % layout)
+    assert_same_bits(fn(a[3000:3001], b), full[3000:3001], "%s row 3000 alone" % layout)
+    rows = [0, 1000, 4095]
+    cols = np.r_[0:32, 2568:2600]
+    if layout == "linear":
+        ref, nrm = oracle.linear(a[rows].cpu(), b[cols].cpu())
+    else:
+        ref, nrm = oracle.matmul(a[rows].cpu(), b[:, cols].contiguous().cpu())
+    check_close(full[rows][:, cols], ref, nrm, torch.bfloat16, "pair %s 4096 rows" % layout)
+    _no_device_error(bi)
