@@ -71,6 +71,9 @@ namespace {
 constexpr int S2_ROWS = 128;       // rows per query tile
 constexpr int S2_KST = 2;          // K ring depth
 constexpr int S2_VST = 2;          // V ring depth
+// The slot releases are the MMA's completion barriers sfull[j & 1] and pvdone[i & 1],
+// so each ring has as many slots as those barriers have entries.
+static_assert(S2_KST == 2 && S2_VST == 2, "ring depth tied to the completion barriers");
 constexpr int S2_THREADS = 320;
 constexpr uint32_t S2_QPANEL = S2_ROWS * 128;     // 16 KB: 128 rows x 64 elements
 constexpr float S2_LAG = 8.0f;     // how far a row's shift may lag its running maximum (log2)
@@ -90,8 +93,8 @@ struct S2Smem {
     static constexpr uint32_t MX = P + PB;                       // float[2][128] half maxima
     static constexpr uint32_t LS = MX + 2 * 128 * 4;             // float[2][128] half sums
     static constexpr uint32_t BARS = LS + 2 * 128 * 4;
-    // bar_q kvfull[2] kempty[2] vempty[2] sfull[2] pfull pvdone mma_done
-    static constexpr uint32_t NBARS = 1 + 2 + S2_KST + S2_VST + 2 + 3;
+    // bar_q kvfull[2] sfull[2] pfull pvdone[2] mma_done
+    static constexpr uint32_t NBARS = 1 + 2 + 2 + 1 + 2 + 1;
     static constexpr uint32_t MISC = BARS + NBARS * 8;           // tmem slot, abort flag
     static constexpr uint32_t END = MISC + 16;
     static constexpr size_t BYTES = 1024 + END;
@@ -128,12 +131,13 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S2Smem::BARS);
     uint64_t *bar_q = bars;
     uint64_t *kvfull = bar_q + 1;        // [2] step j: K_j and V_{j-1} have landed
-    uint64_t *kempty = kvfull + 2;
-    uint64_t *vempty = kempty + S2_KST;
-    uint64_t *sfull = vempty + S2_VST;   // [2]
+    // S(j) done: S buffer j & 1 written, and K slot j % 2 read (the producer's
+    // release too)
+    uint64_t *sfull = kvfull + 2;        // [2]
     uint64_t *pfull = sfull + 2;         // P_j in smem and O rescaled for chunk j
-    uint64_t *pvdone = pfull + 1;        // P_j V_j added into O (P free, O readable)
-    uint64_t *mma_done = pvdone + 1;
+    // P_i V_i added into O, i.e. P free, O readable, V slot i % 2 read: [i & 1]
+    uint64_t *pvdone = pfull + 1;        // [2]
+    uint64_t *mma_done = pvdone + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S2Smem::MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S2Smem::MISC + 4);
 
@@ -158,13 +162,12 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
     if (threadIdx.x == 0) {
         mbar_init(bar_q, 1);
         for (int s = 0; s < 2; ++s) mbar_init(&kvfull[s], 1);
-        for (int s = 0; s < S2_KST; ++s) mbar_init(&kempty[s], 1);
-        for (int s = 0; s < S2_VST; ++s) mbar_init(&vempty[s], 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sfull[i], 1);
         }
         mbar_init(pfull, 8);
-        mbar_init(pvdone, 1);
+        mbar_init(&pvdone[0], 1);
+        mbar_init(&pvdone[1], 1);
         mbar_init(mma_done, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -191,19 +194,21 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
                 tma_load_4d(sQ + pn * S2_QPANEL, &tmQ, bar_q, 64 * pn, kvh * G, qi0, b);
             // Step j loads K_j and V_{j-1} onto one barrier, so that the MMA thread
             // waits once per chunk for both (each wait costs the tensor pipe time).
-            // Every step, the last one (V only) included, first waits for the K slot
-            // release of step j-2 (S(j-2) done): the MMA thread issues S(j-2) only
-            // after its wait on step j-2, which used this same barrier, so the barrier
-            // is never armed again before that phase has been consumed.
+            // Every step, the last one (V only) included, first waits for S(j-2)
+            // (K slot j % 2 read): the MMA thread issues S(j-2) only after its wait
+            // on step j-2, which used this same barrier, so the barrier is never
+            // armed again before that phase has been consumed.  The V slot waits for
+            // P_{j-3} V_{j-3}.  Both are the MMA's own completion barriers, so it
+            // commits twice per chunk, not four times.
             int armed = 0;
             bool ok = true;
             for (int j = 0; j <= nchunks; ++j) {
                 const bool has_k = j < nchunks, has_v = j >= 1;
-                if (!mbar_wait(&kempty[j % S2_KST], ((j / S2_KST) & 1u) ^ 1u, abort_flag)) {
+                if (!mbar_wait(&sfull[j & 1], ((j >> 1) & 1u) ^ 1u, abort_flag)) {
                     ok = false;
                     break;
                 }
-                if (has_v && !mbar_wait(&vempty[(j - 1) % S2_VST], (((j - 1) / S2_VST) & 1u) ^ 1u,
+                if (has_v && !mbar_wait(&pvdone[(j - 1) & 1], (((j - 1) >> 1) & 1u) ^ 1u,
                                         abort_flag)) {
                     ok = false;
                     break;
@@ -254,7 +259,6 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
                                    smem_desc(k_addr + (kk >> 2) * S2_KPANEL + (kk & 3) * 32, 16, 1024),
                                    IDESC_S, kk > 0 ? 1u : 0u);
                     }
-                    mma_commit(&kempty[sk]);
                     mma_commit(&sfull[sb]);
                 }
                 if (j >= 1) {
@@ -272,8 +276,7 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
                                    smem_desc(v_addr + kk * 2048, S2_KPANEL, 1024), IDESC_PV,
                                    (i > 0 || kk > 0) ? 1u : 0u);
                     }
-                    mma_commit(&vempty[sv]);
-                    mma_commit(pvdone);
+                    mma_commit(&pvdone[i & 1]);
                 }
             }
             mma_commit(mma_done);
@@ -373,7 +376,7 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
             const float lsum = __fadd_rn(__fadd_rn(ls01.x, ls01.y), __fadd_rn(ls23.x, ls23.y));
             // P_j and the rescaled O must wait until P_{j-1} V_{j-1} is added in
             if (j >= 1) {
-                warp_wait(pvdone, (j - 1) & 1u, abort_flag);
+                warp_wait(&pvdone[(j - 1) & 1], ((j - 1) >> 1) & 1u, abort_flag);
                 tc_fence_after();
             }
             if (warp_valid) {
@@ -413,7 +416,7 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
             }
         }
         // the last P V, then o = acc / l
-        warp_wait(pvdone, (nchunks - 1) & 1u, abort_flag);
+        warp_wait(&pvdone[(nchunks - 1) & 1], ((nchunks - 1) >> 1) & 1u, abort_flag);
         tc_fence_after();
         if (warp_valid) {
             T *orow = static_cast<T *>(args.o) + b * args.os[0] + h * args.os[1] +
