@@ -359,18 +359,30 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
             float2 ls01 = make_float2(0.0f, 0.0f), ls23 = make_float2(0.0f, 0.0f);
             if (warp_valid) {
                 const float2 c2 = make_float2(sl2, sl2), nm2 = make_float2(-m_new, -m_new);
+                // Two copies of the loop, so that the common (unmasked) one has no
+                // test between the exponentials; both do the same arithmetic.
+                if (full) {
 #pragma unroll
-                for (int i = 0; i < HK; i += 2) {
-                    const float2 t = __ffma2_rn(make_float2(x[i], x[i + 1]), c2, nm2);
-                    float e0 = ex2_approx(t.x), e1 = ex2_approx(t.y);
-                    if (!full) {
+                    for (int i = 0; i < HK; i += 2) {
+                        const float2 t = __ffma2_rn(make_float2(x[i], x[i + 1]), c2, nm2);
+                        const float e0 = ex2_approx(t.x), e1 = ex2_approx(t.y);
+                        x[i] = e0;
+                        x[i + 1] = e1;
+                        if ((i & 2) == 0) ls01 = __fadd2_rn(ls01, make_float2(e0, e1));
+                        else ls23 = __fadd2_rn(ls23, make_float2(e0, e1));
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < HK; i += 2) {
+                        const float2 t = __ffma2_rn(make_float2(x[i], x[i + 1]), c2, nm2);
+                        float e0 = ex2_approx(t.x), e1 = ex2_approx(t.y);
                         if (ARR ? ((vis >> i) & 1u) == 0 : i >= lim) e0 = 0.0f;
                         if (ARR ? ((vis >> (i + 1)) & 1u) == 0 : i + 1 >= lim) e1 = 0.0f;
+                        x[i] = e0;
+                        x[i + 1] = e1;
+                        if ((i & 2) == 0) ls01 = __fadd2_rn(ls01, make_float2(e0, e1));
+                        else ls23 = __fadd2_rn(ls23, make_float2(e0, e1));
                     }
-                    x[i] = e0;
-                    x[i + 1] = e1;
-                    if ((i & 2) == 0) ls01 = __fadd2_rn(ls01, make_float2(e0, e1));
-                    else ls23 = __fadd2_rn(ls23, make_float2(e0, e1));
                 }
             }
             const float lsum = __fadd_rn(__fadd_rn(ls01.x, ls01.y), __fadd_rn(ls23.x, ls23.y));
