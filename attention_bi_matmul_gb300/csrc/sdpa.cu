@@ -85,22 +85,23 @@ struct S2Smem {
     static constexpr uint32_t KPANEL = C * 128;                  // C keys x 64 elements
     static constexpr uint32_t QB = NP * S2_QPANEL;
     static constexpr uint32_t KV = NP * KPANEL;                  // one K or V chunk
-    static constexpr uint32_t PB = S2_ROWS * C * 2;              // P: 128 rows x C keys
     static constexpr uint32_t Q = 0;
     static constexpr uint32_t K = Q + QB;
     static constexpr uint32_t V = K + S2_KST * KV;
-    static constexpr uint32_t P = V + S2_VST * KV;
-    static constexpr uint32_t MX = P + PB;                       // float[2][128] half maxima
+    static constexpr uint32_t MX = V + S2_VST * KV;              // float[2][128] half maxima
     static constexpr uint32_t LS = MX + 2 * 128 * 4;             // float[2][128] half sums
     static constexpr uint32_t BARS = LS + 2 * 128 * 4;
-    // bar_q kvfull[2] sfull[2] pfull pvdone[2] mma_done
-    static constexpr uint32_t NBARS = 1 + 2 + 2 + 1 + 2 + 1;
+    // bar_q kvfull[2] sfull[2] pfull[2] pvdone[2] mma_done
+    static constexpr uint32_t NBARS = 1 + 2 + 2 + 2 + 2 + 1;
     static constexpr uint32_t MISC = BARS + NBARS * 8;           // tmem slot, abort flag
     static constexpr uint32_t END = MISC + 16;
     static constexpr size_t BYTES = 1024 + END;
-    // tensor memory: S0 [0, C), S1 [C, 2C), O [2C, 2C + DP)
+    // tensor memory: S0 [0, C), S1 [C, 2C), O [2C, 2C + DP), then P0 and P1 of C/2
+    // columns each (C keys of the input dtype, two to a column)
     static constexpr uint32_t O_COL = 2 * C;
-    static constexpr uint32_t TMEM_COLS = 2 * C + DP <= 256 ? 256 : 512;
+    static constexpr uint32_t P_COL = 2 * C + DP;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static_assert(P_COL + C <= TMEM_COLS, "tensor memory");
 };
 
 template <typename T, bool ARR, int DP, int C>
@@ -112,10 +113,12 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
     constexpr uint32_t S2_KPANEL = S2Smem::KPANEL;
     constexpr uint32_t S2_KV = S2Smem::KV;
     constexpr uint32_t S2_O_COL = S2Smem::O_COL;
+    constexpr uint32_t S2_P_COL = S2Smem::P_COL;
     constexpr uint32_t S2_TMEM_COLS = S2Smem::TMEM_COLS;
     constexpr int S2_C = C;
     constexpr int HK = C / 2;            // keys per row warp
     constexpr int HD = DP / 2;           // output columns per row warp
+    static_assert(HK == 64 || HK == 32, "P store: 32 or 16 columns per row warp");
     constexpr uint32_t IDESC_S = mma_idesc(IsBf16<T>::value, S2_ROWS, C, false);
     constexpr uint32_t IDESC_PV = mma_idesc(IsBf16<T>::value, S2_ROWS, DP, true);
 
@@ -125,7 +128,6 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
     uint8_t *sQ = smem + S2Smem::Q;
     uint8_t *sK = smem + S2Smem::K;
     uint8_t *sV = smem + S2Smem::V;
-    uint8_t *sP = smem + S2Smem::P;
     float *mx_s = reinterpret_cast<float *>(smem + S2Smem::MX);
     float *ls_s = reinterpret_cast<float *>(smem + S2Smem::LS);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S2Smem::BARS);
@@ -134,9 +136,14 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
     // S(j) done: S buffer j & 1 written, and K slot j % 2 read (the producer's
     // release too)
     uint64_t *sfull = kvfull + 2;        // [2]
-    uint64_t *pfull = sfull + 2;         // P_j in smem and O rescaled for chunk j
-    // P_i V_i added into O, i.e. P free, O readable, V slot i % 2 read: [i & 1]
-    uint64_t *pvdone = pfull + 1;        // [2]
+    // [j & 1]: P_j in tensor memory and O rescaled for chunk j.  Two barriers, not one:
+    // a row warp with no valid rows may arrive for chunk j + 1 (S(j + 1) is issued
+    // before the MMA thread waits for P_j) before the others arrive for chunk j, and
+    // one barrier would then count that arrival towards chunk j.  It cannot get two
+    // chunks ahead: S(j + 2) is issued only after P_j's barrier has completed.
+    uint64_t *pfull = sfull + 2;         // [2]
+    // P_i V_i added into O, i.e. P buffer i & 1 free, O readable, V slot i % 2 read: [i & 1]
+    uint64_t *pvdone = pfull + 2;        // [2]
     uint64_t *mma_done = pvdone + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S2Smem::MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S2Smem::MISC + 4);
@@ -165,7 +172,8 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sfull[i], 1);
         }
-        mbar_init(pfull, 8);
+        mbar_init(&pfull[0], 8);
+        mbar_init(&pfull[1], 8);
         mbar_init(&pvdone[0], 1);
         mbar_init(&pvdone[1], 1);
         mbar_init(mma_done, 1);
@@ -240,7 +248,6 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
             // ------------------------------------------------ MMA issuer
             bool ok = mbar_wait(bar_q, 0, abort_flag);
             const uint32_t q_addr = smem_u32(sQ);
-            const uint32_t p_addr = smem_u32(sP);
             for (int j = 0; ok && j <= nchunks; ++j) {
                 // step j: K_j (if j < nchunks) and V_{j-1} (if j >= 1) have landed
                 if (!mbar_wait(&kvfull[j & 1], (j >> 1) & 1u, abort_flag)) { ok = false; break; }
@@ -265,14 +272,15 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
                     // O (+)= P_i V_i, i = j - 1 (the rows rescaled O before signalling)
                     const int i = j - 1;
                     const uint32_t sv = i % S2_VST;
-                    if (!mbar_wait(pfull, i & 1u, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(&pfull[i & 1], (i >> 1) & 1u, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t v_addr = smem_u32(sV + sv * S2_KV);
 #pragma unroll
                     for (int kk = 0; kk < C / 16; ++kk) {
-                        // P: 64-key panels of 128 rows; V: MN-major, 64-column atoms
-                        mma_f16_ss(tmem_base + S2_O_COL,
-                                   smem_desc(p_addr + (kk >> 2) * S2_QPANEL + (kk & 3) * 32, 16, 1024),
+                        // P from tensor memory (8 columns per 16 keys); V: MN-major,
+                        // 64-column atoms
+                        mma_f16_ts(tmem_base + S2_O_COL,
+                                   tmem_base + S2_P_COL + (i & 1) * (C / 2) + kk * 8,
                                    smem_desc(v_addr + kk * 2048, S2_KPANEL, 1024), IDESC_PV,
                                    (i > 0 || kk > 0) ? 1u : 0u);
                     }
@@ -386,40 +394,38 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
                 }
             }
             const float lsum = __fadd_rn(__fadd_rn(ls01.x, ls01.y), __fadd_rn(ls23.x, ls23.y));
-            // P_j and the rescaled O must wait until P_{j-1} V_{j-1} is added in
-            if (j >= 1) {
+            // P_j goes to P buffer j & 1, which held P_{j-2}.  P_{j-2} V_{j-2} is
+            // complete: the MMA thread issued it before S(j), and S(j)'s commit (waited
+            // for above) arrives only once every MMA issued before it has completed.
+            if (warp_valid) {
+                // keys HK*half.. of row r, two to a 32-bit column (lower key in the low half)
+                uint32_t pw[HK / 2];
+#pragma unroll
+                for (int w = 0; w < HK / 2; ++w) pw[w] = cvt2<T>(x[2 * w], x[2 * w + 1]);
+                const uint32_t p_addr = tmem_base + lane_base + S2_P_COL + sb * (C / 2) + half * (HK / 2);
+                if constexpr (HK == 64) tmem_st32(p_addr, pw);
+                else tmem_st16(p_addr, pw);
+            }
+            // O *= alpha for this warp's HD columns, after P_{j-1} V_{j-1} is added in
+            // (skipped, wait included, when every row has alpha 1)
+            if (j >= 1 && warp_valid && __any_sync(0xffffffffu, alpha != 1.0f)) {
                 warp_wait(&pvdone[(j - 1) & 1], ((j - 1) >> 1) & 1u, abort_flag);
                 tc_fence_after();
-            }
-            if (warp_valid) {
-                // keys HK*half.. of row r: 64-key panels of 128-byte rows, 16-byte chunks
-#pragma unroll
-                for (int cc = 0; cc < HK / 8; ++cc) {
-                    const int key = half * HK + cc * 8;
-                    const uint4 v = pack8x2<T>(x + cc * 8);
-                    uint8_t *dst = sP + (key >> 6) * S2_QPANEL + r * 128 +
-                                   ((((key & 63) >> 3) ^ (r & 7)) << 4);
-                    *reinterpret_cast<uint4 *>(dst) = v;
-                }
-                fence_proxy_async_smem();
-                // O *= alpha for this warp's HD columns (skipped when every row has alpha 1)
-                if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.0f)) {
 #pragma unroll 1
-                    for (int c4 = 0; c4 < HD / 32; ++c4) {
-                        uint32_t ov[32];
-                        tmem_ld32(o_addr + c4 * 32, ov);
-                        tmem_wait_ld(ov);
+                for (int c4 = 0; c4 < HD / 32; ++c4) {
+                    uint32_t ov[32];
+                    tmem_ld32(o_addr + c4 * 32, ov);
+                    tmem_wait_ld(ov);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            ov[e] = __float_as_uint(__fmul_rn(__uint_as_float(ov[e]), alpha));
-                        tmem_st32(o_addr + c4 * 32, ov);
-                    }
-                    tmem_wait_st();
+                    for (int e = 0; e < 32; ++e)
+                        ov[e] = __float_as_uint(__fmul_rn(__uint_as_float(ov[e]), alpha));
+                    tmem_st32(o_addr + c4 * 32, ov);
                 }
             }
+            if (warp_valid) tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(pfull);
+            if (lane == 0) mbar_arrive(&pfull[sb]);
             ls_s[half * 128 + r] = lsum;
             pair_sync(quarter);
             if (any) {
