@@ -261,6 +261,69 @@ def capture(parts, bi):
     return graphs, bi.launch_count() - n0
 
 
+def cost_of_invariance(wl, dev, blocks=5, reps=10):
+    """The library's parts against torch / cuBLAS on the same inputs: each part and its
+    torch equivalent captured as CUDA graphs and timed in alternating blocks; medians.
+    Prefill attention (causal, B4 H32 Hkv8 L4096 D128) is added beside the step's parts."""
+    import statistics
+    import torch
+    import torch.nn.functional as F
+    import attention_bi_matmul_gb300 as bi
+    from attention_bi_matmul_gb300 import synth
+
+    def torch_sweep():
+        i = 0
+        for N in C2_N:
+            for M in C2_M:
+                torch.mm(wl.x[:M], wl.w[N][i % WCOPIES].t(), out=wl.y[N][:M])
+                i += 1
+
+    B, H, Hkv, D, L = 4, 32, 8, 128, 4096
+    qp, kp, vp = synth.sdpa_qkv(B, H, Hkv, L, L, D, "bf16", seed=11, device=dev)
+    op = torch.empty_like(qp)
+    cases = {
+        "batch_sweep": (lambda: wl.part_batch_sweep(bi), torch_sweep),
+        "gemm_8192": (lambda: wl.part_gemm(bi), lambda: torch.mm(wl.X, wl.W.t(), out=wl.Y)),
+        # one query at the end of the cache sees every key: torch's unmasked form
+        "sdpa_decode": (lambda: wl.part_sdpa(bi),
+                        lambda: F.scaled_dot_product_attention(wl.q, wl.k, wl.v, enable_gqa=True)),
+        "sdpa_prefill_b4_l4096": (lambda: bi.sdpa(qp, kp, vp, causal=True, q_offset=0, out=op),
+                                  lambda: F.scaled_dot_product_attention(qp, kp, vp, is_causal=True,
+                                                                         enable_gqa=True)),
+    }
+    out = {}
+    for name, fns in cases.items():
+        graphs = []
+        for fn in fns:
+            fn()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn()
+            g.replay()
+            graphs.append(g)
+        torch.cuda.synchronize()
+        t = ([], [])
+        for _ in range(blocks):
+            for which, g in enumerate(graphs):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for _ in range(reps):
+                    g.replay()
+                e1.record()
+                torch.cuda.synchronize()
+                t[which].append(e0.elapsed_time(e1) / reps)
+        ours, ref = statistics.median(t[0]), statistics.median(t[1])
+        out[name] = {"ours_ms": round(ours, 4), "torch_ms": round(ref, 4), "ratio": round(ours / ref, 3)}
+        del graphs
+    del qp, kp, vp, op
+    out["method"] = ("each part and its torch equivalent (torch.mm on cuBLAS; "
+                     "F.scaled_dot_product_attention with enable_gqa) on the same inputs, captured "
+                     "as CUDA graphs and timed in %d alternating blocks of %d replays; medians; "
+                     "ratio = ours / torch (below 1: the invariant kernel is faster)" % (blocks, reps))
+    return out
+
+
 def batch_sweep_per_call(wl, bi, hbm, reps=10, calls=8):
     """Device time per call of each batch-sweep shape: a graph of `calls` back-to-back calls
     cycling through the 4 weight copies, replayed `reps` times (as the step issues them)."""
@@ -478,6 +541,8 @@ def run_ours(args):
     if st != 0:
         raise RuntimeError("device error word %#x after the timed region" % code)
     per_call = batch_sweep_per_call(wl, bi, hbm) if args.per_call else None
+    step_ms = [ev[s][0].elapsed_time(ev[s][len(parts)]) for s in range(K)]
+    coi = cost_of_invariance(wl, dev) if rank == 0 and not args.no_torch_compare else None
 
     flops = step_flops()
     byts = step_bytes()
@@ -550,6 +615,8 @@ def run_ours(args):
                             "each part captured once as a CUDA graph, replayed every step")
         out = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
                "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+               "ms_per_step_median": round(statistics.median(step_ms), 4),
+               "step_ms_samples": [round(x, 4) for x in step_ms],
                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
                "data": "synthetic (seeded torch CUDA generator; shapes and distributions of the "
                        "configs)",
@@ -559,7 +626,7 @@ def run_ours(args):
                        "d2h_bytes_per_step": d2h, "same_bits_as_device_run": e2e_same,
                        "overlap": "inputs copied per part on a copy stream, results read back "
                                   "on another while later parts' inputs arrive"},
-               "gpu_launches": launches, "clocks": clocks,
+               "gpu_launches": launches, "clocks": clocks, "cost_of_invariance": coi,
                "batch_sweep_per_call": per_call}
         emit(out, rank)
     if world > 1:
@@ -650,12 +717,14 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip timing the CPU oracle (for profiling runs)")
     ap.add_argument("--budget-s", type=float, default=0.0,
                     help="reference arm: CPU seconds per step (default: fit the run in ~2.5 min)")
+    ap.add_argument("--no-torch-compare", action="store_true",
+                    help="skip the comparison with torch / cuBLAS on the same inputs")
     ap.add_argument("--per-call", action="store_true",
                     help="also report the device time of every batch-sweep shape")
     ap.add_argument("--eager", action="store_true",
