@@ -163,6 +163,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     constexpr uint32_t TMEM_COLS = tc_tmem_cols(BN);
     constexpr uint32_t IDESC = mma_idesc(IsBf16<T>::value, TC_BM, BN, B_MN);
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile width");
+    constexpr int EB = BN / 32 < 4 ? BN / 32 : 4;       // epilogue loads per wait
     static_assert(!B_MN || BN % 64 == 0, "MN-major B needs 64-column atoms");
 
     extern __shared__ uint8_t smem_raw[];
@@ -198,6 +199,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int KB = static_cast<int>((K + KP * TC_BK - 1) / (KP * TC_BK));   // stages per tile
 
     if (threadIdx.x == 0) {
+        // fetch the copy descriptors while the block sets up (the first copy waits for them)
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
@@ -222,8 +226,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
-            prefetch_tmap(&tmA);
-            prefetch_tmap(&tmB);
             // The A copy moves only the rows that exist (a_rows <= 128); tile rows past
             // them are never stored, and no row's result depends on another row.
             const uint32_t tx = KP * (static_cast<uint32_t>(args.a_rows) * TC_BK * 2 + B_PANEL);
@@ -337,12 +339,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             if (!warp_wait(&tfull[acc], aph, abort_flag)) break;
             tc_fence_after();
             const int64_t m = mb * TC_BM + row_in_tile;
+            // EB 32-column loads in flight per wait (the wait's latency, not the
+            // bandwidth, bounds a tile's epilogue)
 #pragma unroll 1
-            for (int cc = 0; cc < BN / 32; ++cc) {
-                uint32_t r[32];
-                tmem_ld32(tmem_base + ((quarter * 32u) << 16) + acc * BN + cc * 32, r);
-                tmem_wait_ld(r);
-                if (m < M) gemm_epilogue32<T>(r, e, m, nb * BN + cc * 32, args);
+            for (int c0 = 0; c0 < BN / 32; c0 += EB) {
+                uint32_t r[EB][32];
+#pragma unroll
+                for (int u = 0; u < EB; ++u)
+                    tmem_ld32(tmem_base + ((quarter * 32u) << 16) + acc * BN + (c0 + u) * 32, r[u]);
+                tmem_wait_ld(r[0]);
+#pragma unroll
+                for (int u = 1; u < EB; ++u) tmem_tie(r[u]);
+                if (m < M) {
+#pragma unroll
+                    for (int u = 0; u < EB; ++u)
+                        gemm_epilogue32<T>(r[u], e, m, nb * BN + (c0 + u) * 32, args);
+                }
             }
             tc_fence_before();
             __syncwarp();
@@ -401,6 +413,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     constexpr uint32_t TMEM_COLS = tc_tmem_cols(BN);
     constexpr uint32_t IDESC = mma_idesc(IsBf16<T>::value, TC2_BM, BN, B_MN);
     static_assert(BN == 128 || BN == 256, "pair tile width");
+    constexpr int EB = 2;                                // epilogue loads per wait
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -435,6 +448,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     const int64_t pair = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
 
     if (threadIdx.x == 0) {
+        // fetch the copy descriptors while the block sets up (the first copy waits for them)
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
@@ -460,8 +476,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer (both CTAs)
-            prefetch_tmap(&tmA);
-            prefetch_tmap(&tmB);
             const uint32_t tx = 2u * (A_BYTES + B_BYTES);       // both CTAs' bytes
             uint32_t it = 0, s = 0, ph = 0;
             bool ok = true;
@@ -560,12 +574,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
             if (!warp_wait(&tfull[acc], aph, abort_flag)) break;
             tc_fence_after();
             const int64_t m = mb * TC2_BM + row_in_tile;
+            // EB 32-column loads in flight per wait (the wait's latency, not the
+            // bandwidth, bounds a tile's epilogue)
 #pragma unroll 1
-            for (int cc = 0; cc < BN / 32; ++cc) {
-                uint32_t r[32];
-                tmem_ld32(tmem_base + ((quarter * 32u) << 16) + acc * BN + cc * 32, r);
-                tmem_wait_ld(r);
-                if (m < M) gemm_epilogue32<T>(r, e, m, nb * BN + cc * 32, args);
+            for (int c0 = 0; c0 < BN / 32; c0 += EB) {
+                uint32_t r[EB][32];
+#pragma unroll
+                for (int u = 0; u < EB; ++u)
+                    tmem_ld32(tmem_base + ((quarter * 32u) << 16) + acc * BN + (c0 + u) * 32, r[u]);
+                tmem_wait_ld(r[0]);
+#pragma unroll
+                for (int u = 1; u < EB; ++u) tmem_tie(r[u]);
+                if (m < M) {
+#pragma unroll
+                    for (int u = 0; u < EB; ++u)
+                        gemm_epilogue32<T>(r[u], e, m, nb * BN + (c0 + u) * 32, args);
+                }
             }
             tc_fence_before();
             __syncwarp();

@@ -438,6 +438,22 @@ __device__ __forceinline__ void tmem_wait_st() {
 
 // Wait for this thread's outstanding tcgen05.ld.  The registers are passed as
 // in/out operands so that the compiler cannot move their uses above the wait.
+// Orders uses of r after an earlier tmem_wait_ld of the same thread: that wait
+// covers every tcgen05.ld the thread issued before it, but names only its own
+// registers; this empty (volatile, so not reordered against the wait) statement
+// names the other batch's.
+__device__ __forceinline__ void tmem_tie(uint32_t (&r)[32]) {
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]),
+                   "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                   "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]),
+                   "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;"
                  : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
