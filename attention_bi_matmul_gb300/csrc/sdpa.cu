@@ -25,8 +25,9 @@
 //     p_j = 2^(fma(s_j, c, -m')); l = l * alpha + (half sum + half sum), each
 //     half summed as four interleaved partial sums (key mod 4) added as
 //     (0+1)+(2+3); P rounded to the input dtype;
-//   * the output is one fp32 accumulator in tensor memory that the P V MMA adds
-//     into: before chunk j's P V, every row rescales it by alpha_j (one fp32
+//   * P is written into tensor memory and read from there by the P V MMA (its A
+//     operand); the output is one fp32 accumulator in tensor memory that the
+//     P V MMA adds into: before chunk j's P V, every row rescales it by alpha_j (one fp32
 //     multiply per element, rounded to nearest).  A warp whose 32 rows all have
 //     alpha = 1 skips the rescale: multiplying by 1 is exact, so the bits do
 //     not depend on which rows share the warp.  2^x is the hardware's
@@ -46,10 +47,9 @@
 //
 // Roles (320 threads):
 //   warp 0 lane 0   TMA producer (Q once; K and V chunks through 2-deep rings)
-//   warp 1          TMEM allocation (S0, S1 of C columns, O of DP); lane 0
-//                   issues the MMAs, waiting twice per chunk (K_j with V_{j-1},
-//                   then P_{j-1}): every barrier wait of the issuing thread leaves
-//                   the tensor pipe idle for a few hundred cycles
+//   warp 1          TMEM allocation (S0, S1 of C columns, O of DP, P0, P1 of
+//                   C/2); lane 0 issues the MMAs, waiting twice per chunk (K_j
+//                   with V_{j-1}, then P_{j-1})
 //   warps 2..9      row warps: warp w serves TMEM lane quarter w % 4 and half
 //                   (w-2)/4 of the keys (C/2) and of the output columns (DP/2);
 //                   the two warps of a row exchange the chunk maximum and the
