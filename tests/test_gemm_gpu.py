@@ -193,6 +193,20 @@ def test_rows_invariant_wide_tile_k8192(bi, dt):
     check_close(full[rows][:, cols], ref, nrm, DT[dt], "K=8192 sampled")
 
 
+def test_linear_8192_cube_full_size_sampled(bi):
+    """The bench's large GEMM at full size and in the bench's launch form (bi_linear, CTA
+    pairs, two K panels per stage, more tiles than resident pairs): sampled outputs from
+    every corner and the middle against the oracle, and the same bits on a second call."""
+    x, w = synth.gemm16(8192, 8192, 8192, "bf16", seed=21, layout="linear", device="cuda")
+    y = bi.linear(x, w)
+    rows = [0, 1, 127, 128, 4095, 4096, 8190, 8191]
+    cols = np.r_[0:32, 4080:4112, 8160:8192]
+    ref, nrm = oracle.linear(x[rows].cpu(), w[cols].contiguous().cpu())
+    check_close(y[rows][:, cols], ref, nrm, torch.bfloat16, "8192^3 linear sampled")
+    assert_same_bits(bi.linear(x, w), y, "8192^3 linear, second call")
+    _no_device_error(bi)
+
+
 def test_c2_cublas_control_differs(bi):
     """The negative control: torch.matmul (cuBLAS) changes a row's bits with the batch size
     on at least one of the config's shapes, where the library's do not."""
