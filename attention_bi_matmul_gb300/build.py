@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libbi.so")
 
-SOURCES = ["api.cu", "gemm_f32.cu", "gemm_tc_bf16.cu", "gemm_tc_f16.cu", "sdpa.cu", "sdpa_pair.cu", "glue.cu",
+SOURCES = ["api.cu", "gemm_f32.cu", "gemm_tc_bf16.cu", "gemm_tc_f16.cu", "sdpa.cu", "glue.cu",
            "qgemm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE]

@@ -119,7 +119,6 @@ bi_status device_init(int dev) {
     if ((st = init_gemm_tc_bf16()) != BI_OK) return st;
     if ((st = init_gemm_tc_f16()) != BI_OK) return st;
     if ((st = init_sdpa()) != BI_OK) return st;
-    if ((st = init_sdpa_pair()) != BI_OK) return st;
     if ((st = init_qgemm()) != BI_OK) return st;
     if (!device_error_word()) return BI_ERR_CUDA;
     device_sm_count();

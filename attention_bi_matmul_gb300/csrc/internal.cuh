@@ -54,7 +54,6 @@ bi_status cuda_status(cudaError_t e);
 bi_status init_gemm_tc_bf16();
 bi_status init_gemm_tc_f16();
 bi_status init_sdpa();
-bi_status init_sdpa_pair();
 bi_status init_qgemm();
 
 // ---- launchers
@@ -97,11 +96,6 @@ struct SdpaArgs {
 };
 bi_status launch_sdpa(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                       const SdpaArgs &args, bi_dtype dt, cudaStream_t s);
-// Two query tiles per block (sdpa_pair.cu): launched, and *used set, only for calls
-// with at least two query tiles on the shapes it is built for; the rows' bits are the
-// one-tile kernel's.
-bi_status launch_sdpa_pair(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                           const SdpaArgs &args, bi_dtype dt, cudaStream_t s, bool *used);
 
 bi_status launch_rmsnorm(const void *x, int64_t ldx, const void *w, void *y, int64_t ldy,
                          int64_t M, int64_t N, float eps, bi_dtype dt, cudaStream_t s);

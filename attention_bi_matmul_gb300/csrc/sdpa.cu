@@ -526,11 +526,6 @@ bi_status init_sdpa() {
 
 bi_status launch_sdpa(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                       const SdpaArgs &args, bi_dtype dt, cudaStream_t s) {
-    // Calls with two or more query tiles go to the two-tile kernel where it is built:
-    // a scheduling choice only, every row's bits are this kernel's.
-    bool used = false;
-    const bi_status pst = launch_sdpa_pair(tq, tk, tv, args, dt, s, &used);
-    if (pst != BI_OK || used) return pst;
     if (dt == BI_BF16) return s2_shape<__nv_bfloat16>(tq, tk, tv, args, s);
     if (dt == BI_F16) return s2_shape<__half>(tq, tk, tv, args, s);
     return BI_ERR_UNSUPPORTED;

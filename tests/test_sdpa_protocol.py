@@ -259,187 +259,3 @@ def test_protocol_holds(pattern):
 def test_planted_protocol_mistakes_are_caught(mutation):
     with pytest.raises(Hazard):
         run_many(PATTERNS, range(2, 11), range(40), **{mutation: True})
-
-
-# ------------------------------------------------------------------ two query tiles per block
-
-class PairModel(Model):
-    """The two-tile form: query tiles a and b (b may be absent) share the K/V ring; each
-    has one S buffer in tensor memory, which its P overwrites, and its own O; one row warp
-    per lane quarter and tile (four per tile).  The MMA thread, per step j: for each tile,
-    P V(j-1) then -- once that has completed -- S(j); then one commit that frees the K
-    slot (both tiles' S) and one that frees the V slot (both tiles' P V)."""
-
-    def __init__(self, n, valid_a, valid_b, rng, no_pv_wait=False, early_kfree=False):
-        super().__init__(n, [True] * 8, rng)
-        self.tiles = ["a"] + (["b"] if valid_b is not None else [])
-        self.tvalid = {"a": valid_a, "b": valid_b}
-        self.no_pv_wait, self.early_kfree = no_pv_wait, early_kfree
-        B = Barrier
-        self.kfree = [B("kfree0", 1), B("kfree1", 1)]
-        self.vfree = [B("vfree0", 1), B("vfree1", 1)]
-        self.tsfull = {t: B("sfull_" + t, 1) for t in self.tiles}
-        self.tpfull = {t: B("pfull_" + t, 4) for t in self.tiles}
-        self.tpvdone = {t: B("pvdone_" + t, 1) for t in self.tiles}
-        self.pfull = list(self.tpfull.values())
-        self.ts_done = {t: set() for t in self.tiles}
-        self.tpv_done = {t: set() for t in self.tiles}
-        self.ts_read = {t: {} for t in self.tiles}
-        self.tp_written = {t: {} for t in self.tiles}
-
-    def producer(self):
-        n = self.n
-        self.pending.append((self.bar_q, lambda: self.landed.add("Q")))
-        yield "step"
-        for j in range(n + 1):
-            yield from self.wait(self.kfree[j & 1], ((j >> 1) & 1) ^ 1, (j >> 1) - 1, "producer")
-            if j >= 1:
-                yield from self.wait(self.vfree[(j - 1) & 1], (((j - 1) >> 1) & 1) ^ 1, ((j - 1) >> 1) - 1,
-                                     "producer")
-            for t in self.tiles:
-                if j < n and j >= 2:
-                    self.need(j - 2 in self.ts_done[t], "K slot refilled before S_%s(%d) read it" % (t, j - 2))
-                if j >= 3:
-                    self.need(j - 3 in self.tpv_done[t], "V slot refilled before P V_%s(%d) read it" % (t, j - 3))
-
-            def land(j=j):
-                if j < n:
-                    self.landed.add(("K", j))
-                if j >= 1:
-                    self.landed.add(("V", j - 1))
-            self.pending.append((self.kvfull[j & 1], land))
-            yield "step"
-
-    def mma(self):
-        n = self.n
-        yield from self.wait(self.bar_q, 0, 0, "mma")
-        for j in range(n + 1):
-            yield from self.wait(self.kvfull[j & 1], (j >> 1) & 1, j >> 1, "mma")
-            for t in self.tiles:
-                if j >= 1:
-                    i = j - 1
-                    yield from self.wait(self.tpfull[t], i & 1, i, "mma")
-                    need = {w for w in range(4) if self.tvalid[t][w]}
-                    got = self.tp_written[t].get(i, set())
-                    self.need(need <= got, "P V_%s(%d) issued before P was written by warps %s" % (t, i, sorted(need - got)))
-                    self.need(("V", i) in self.landed, "P V_%s(%d) issued before V landed" % (t, i))
-                    self.pipe.append(("op", "PV" + t, i))
-                    self.pipe.append(("commit", self.tpvdone[t]))
-                    yield "step"
-                if j < n:
-                    if j >= 1 and not self.no_pv_wait:
-                        yield from self.wait(self.tpvdone[t], (j - 1) & 1, j - 1, "mma")
-                    if j >= 1:
-                        self.need(j - 1 in self.tpv_done[t], "S_%s(%d) overwrites P_%s(%d) before its P V was done"
-                                  % (t, j, t, j - 1))
-                        self.need(len(self.ts_read[t].get(j - 1, ())) == 4, "S_%s(%d) before every row read S(%d)" % (t, j, j - 1))
-                    self.need("Q" in self.landed and ("K", j) in self.landed, "S_%s(%d) before Q/K landed" % (t, j))
-                    self.pipe.append(("op", "S" + t, j))
-                    self.pipe.append(("commit", self.tsfull[t]))
-                    if self.early_kfree and t == "a":
-                        self.pipe.append(("commit", self.kfree[j & 1]))
-                    yield "step"
-            if j < n and not self.early_kfree:
-                self.pipe.append(("commit", self.kfree[j & 1]))
-            if j >= 1:
-                self.pipe.append(("commit", self.vfree[(j - 1) & 1]))
-            yield "step"
-        self.pipe.append(("commit", self.mma_done))
-        yield from self.wait(self.mma_done, 0, 0, "mma")
-
-    def tile_row_warp(self, t, w):
-        n = self.n
-        for j in range(n):
-            yield from self.wait(self.tsfull[t], j & 1, j, "row%s%d" % (t, w))
-            self.need(j in self.ts_done[t], "row %s%d read S(%d) before it was complete" % (t, w, j))
-            self.ts_read[t].setdefault(j, set()).add(w)
-            yield "step"
-            if self.tvalid[t][w]:
-                self.tp_written[t].setdefault(j, set()).add(w)
-                yield "step"
-                key = (t, w, j)
-                if key not in self.rescale:
-                    self.rescale[key] = j >= 1 and self.rng.random() < 0.3
-                if self.rescale[key]:
-                    # no wait of its own: S(j)'s commit followed the MMA thread's wait for P V(j-1)
-                    self.need(j - 1 in self.tpv_done[t], "row %s%d rescaled O before P V(%d) was done" % (t, w, j - 1))
-                    yield "step"
-            self.tpfull[t].arrive(j)
-            yield "step"
-        yield from self.wait(self.tpvdone[t], (n - 1) & 1, n - 1, "row%s%d" % (t, w))
-        self.need(n - 1 in self.tpv_done[t], "row %s%d read O before the last P V" % (t, w))
-
-    def engine_step(self):
-        choices = []
-        if self.pending:
-            choices.append("copy")
-        if self.pipe:
-            choices.append("pipe")
-        if not choices:
-            return False
-        if self.rng.choice(choices) == "copy":
-            bar, act = self.pending.pop(self.rng.randrange(len(self.pending)))
-            act()
-            bar.arrive()
-        else:
-            kind, *rest = self.pipe.pop(0)
-            if kind == "op":
-                name, idx = rest
-                (self.ts_done if name[0] == "S" else self.tpv_done)[name[-1]].add(idx)
-            else:
-                rest[0].arrive()
-        return True
-
-    def run(self, max_steps=400000):
-        agents = [self.producer(), self.mma()] + [self.tile_row_warp(t, w) for t in self.tiles for w in range(4)]
-        live = list(range(len(agents)))
-        for _ in range(max_steps):
-            if not live:
-                break
-            if self.rng.random() < 0.3 and self.engine_step():
-                continue
-            order = live[:]
-            self.rng.shuffle(order)
-            moved = False
-            for a in order:
-                try:
-                    r = next(agents[a])
-                except StopIteration:
-                    live.remove(a)
-                    moved = True
-                    break
-                if r != "blocked":
-                    moved = True
-                    break
-            if not moved and not self.engine_step():
-                raise Hazard("deadlock with agents %s blocked" % live)
-        else:
-            raise Hazard("did not finish")
-        for b in self.pfull:
-            for ph, tags in enumerate(b.phase_tags):
-                self.need(len(set(tags)) == 1, "%s phase %d mixes chunks %s" % (b.name, ph, sorted(set(tags))))
-
-
-PAIR_PATTERNS = {
-    "two full tiles": ([True] * 4, [True] * 4),
-    "one tile (decode, one quarter)": ([True, False, False, False], None),
-    "second tile partly valid": ([True] * 4, [True, True, False, False]),
-}
-
-
-def run_pairs(patterns, chunks, seeds, **kw):
-    for name, (va, vb) in patterns.items():
-        for n in chunks:
-            for seed in seeds:
-                PairModel(n, va, vb, random.Random(7000 * n + seed), **kw).run()
-
-
-@pytest.mark.parametrize("pattern", sorted(PAIR_PATTERNS))
-def test_pair_protocol_holds(pattern):
-    run_pairs({pattern: PAIR_PATTERNS[pattern]}, range(1, 11), range(30))
-
-
-@pytest.mark.parametrize("mutation", ["no_pv_wait", "early_kfree"])
-def test_pair_planted_mistakes_are_caught(mutation):
-    with pytest.raises(Hazard):
-        run_pairs(PAIR_PATTERNS, range(2, 11), range(30), **{mutation: True})

@@ -1,6 +1,7 @@
-"""The two-tile attention kernel (calls with two or more query tiles) against the one-tile
-kernel (calls with one): every row bit for bit, over head dims, group sizes, dtypes and
-all mask forms; and parity with the oracle (GPU)."""
+"""Query-length invariance of attention across head dims, group sizes, dtypes and every
+mask form: the rows of a call spanning several query tiles (both ends ragged) against the
+same rows computed one query tile per call, bit for bit; and a prefill's parity with the
+oracle (GPU)."""
 import pytest
 import torch
 
@@ -59,7 +60,7 @@ def test_rows_same_bits_as_one_tile_calls(bi, D, G, causal):
     q, k, v = synth.sdpa_qkv(B, G * Hkv, Hkv, Lq, Lkv, D, "bf16", seed=D * 31 + G, device="cuda")
     o = bi.sdpa(q, k, v, causal=causal, q_offset=q_offset)
     ref = _tilewise(bi, q, k, v, q_offset, G, causal)
-    assert_same_bits(o, ref, "D=%d G=%d causal=%s: two-tile vs one-tile" % (D, G, causal))
+    assert_same_bits(o, ref, "D=%d G=%d causal=%s: several tiles vs one per call" % (D, G, causal))
     _no_device_error(bi)
 
 
@@ -75,18 +76,18 @@ def test_mask_array_and_sinks_same_bits(bi, dt):
     sk = synth.normal((H,), 79, 2.0, "f32").cuda()
     o = bi.sdpa(q, k, v, mask=m, sinks=sk, q_offset=q_offset)
     ref = _tilewise(bi, q, k, v, q_offset, G, None, mask=m, sinks=sk)
-    assert_same_bits(o, ref, "array mask + sinks: two-tile vs one-tile")
+    assert_same_bits(o, ref, "array mask + sinks: several tiles vs one per call")
     _no_device_error(bi)
 
 
 def test_prefill_parity_and_repeat(bi):
-    """A causal prefill served by the two-tile kernel: sampled rows against the oracle,
-    and the same bits on a second call."""
+    """A causal prefill of many query tiles: sampled rows against the oracle, and the
+    same bits on a second call."""
     B, H, Hkv, L, D = 1, 8, 2, 600, 128
     q, k, v = synth.sdpa_qkv(B, H, Hkv, L, L, D, "bf16", seed=5, device="cuda")
     o = bi.sdpa(q, k, v, causal=True, q_offset=0)
     assert_same_bits(bi.sdpa(q, k, v, causal=True, q_offset=0), o, "second call")
     ref, nrm = oracle.sdpa(q.cpu(), k.cpu(), v.cpu(), causal=True, q_offset=0)
     rows = [0, 1, 31, 32, 300, 598, 599]
-    check_close(o[:, :, rows], ref[:, :, rows], nrm[:, :, rows], torch.bfloat16, "two-tile prefill sampled")
+    check_close(o[:, :, rows], ref[:, :, rows], nrm[:, :, rows], torch.bfloat16, "prefill sampled")
     _no_device_error(bi)
