@@ -301,6 +301,58 @@ __device__ __forceinline__ void mma4_f16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         : "memory");
 }
 
+// 16 (or 8) K = 16 steps with A in tensor memory from one asm block, every A
+// address and B descriptor computed beforehand: no arithmetic between the MMAs, so
+// the issuing thread does not wait for an integer pipe that other warps keep busy.
+// The first step accumulates iff accumulate != 0, the others always.
+__device__ __forceinline__ void mma16_f16_ts(uint32_t d, const uint32_t (&a)[16], const uint64_t (&b)[16],
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, t;\n\t"
+        "setp.ne.b32 p, %34, 0;\n\tsetp.eq.b32 t, %33, %33;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %17, %33, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %18, %33, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %19, %33, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %20, %33, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %21, %33, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], %22, %33, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %23, %33, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%8], %24, %33, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], %25, %33, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%10], %26, %33, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%11], %27, %33, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%12], %28, %33, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%13], %29, %33, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%14], %30, %33, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%15], %31, %33, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%16], %32, %33, t;\n\t}"
+        ::"r"(d), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]),
+        "r"(a[8]), "r"(a[9]), "r"(a[10]), "r"(a[11]), "r"(a[12]), "r"(a[13]), "r"(a[14]), "r"(a[15]),
+        "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]),
+        "l"(b[8]), "l"(b[9]), "l"(b[10]), "l"(b[11]), "l"(b[12]), "l"(b[13]), "l"(b[14]), "l"(b[15]),
+        "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma8_f16_ts(uint32_t d, const uint32_t (&a)[8], const uint64_t (&b)[8],
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, t;\n\t"
+        "setp.ne.b32 p, %18, 0;\n\tsetp.eq.b32 t, %17, %17;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %9, %17, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %10, %17, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %11, %17, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %12, %17, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %13, %17, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], %14, %17, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %15, %17, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%8], %16, %17, t;\n\t}"
+        ::"r"(d), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]),
+        "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]),
+        "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive (once) on `bar` when all previously issued tcgen05.mma of this thread complete.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile(

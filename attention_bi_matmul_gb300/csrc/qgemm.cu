@@ -361,12 +361,32 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
                     tc_fence_after();
                     const uint32_t a_tmem = tmem_base + QG_A_COL + d * QB_B * (QG_K / 2);
                     const uint64_t xd = x_desc0 + ((xs * XBB) >> 4);
-                    // panel b: A columns a_tmem + 32 b (8 per 16 k), x panel b of the batch
-                    mma4_f16_ts(d_tmem, a_tmem, xd, IDESC, p0 != 0 ? 1u : 0u);
+                    // panel b: A columns a_tmem + 32 b (8 per 16 k), x panel b of the batch.
+                    // 4-bit: a whole batch goes out from one asm block with its operands
+                    // computed first (measured 5-7% faster, e.g. 26.6 -> 25.3 us at M = 1,
+                    // N = 14336; flat to 2% slower at 2 and 8 bits, which keep the
+                    // per-panel form).  The same MMAs in the same order either way.
+                    if (BITS == 4 && nb_ == QB_B && (QB_B == 4 || QB_B == 2)) {
+                        uint32_t av[4 * QB_B];
+                        uint64_t bv[4 * QB_B];
 #pragma unroll
-                    for (int b = 1; b < QB_B; ++b)
-                        if (b < nb_)
-                            mma4_f16_ts(d_tmem, a_tmem + b * (QG_K / 2), xd + b * xb16, IDESC, 1u);
+                        for (int b = 0; b < QB_B; ++b)
+#pragma unroll
+                            for (int s4 = 0; s4 < 4; ++s4) {
+                                av[4 * b + s4] = a_tmem + b * (QG_K / 2) + 8 * s4;
+                                bv[4 * b + s4] = xd + b * xb16 + 2 * s4;
+                            }
+                        if constexpr (QB_B == 4)
+                            mma16_f16_ts(d_tmem, av, bv, IDESC, p0 != 0 ? 1u : 0u);
+                        else if constexpr (QB_B == 2)
+                            mma8_f16_ts(d_tmem, av, bv, IDESC, p0 != 0 ? 1u : 0u);
+                    } else {
+                        mma4_f16_ts(d_tmem, a_tmem, xd, IDESC, p0 != 0 ? 1u : 0u);
+#pragma unroll
+                        for (int b = 1; b < QB_B; ++b)
+                            if (b < nb_)
+                                mma4_f16_ts(d_tmem, a_tmem + b * (QG_K / 2), xd + b * xb16, IDESC, 1u);
+                    }
                     mma_commit(&a_empty[d]);
                     mma_commit(&x_empty[xs]);
                     if (++d == DSB) { d = 0; dph ^= 1u; }
