@@ -247,7 +247,38 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
         if (lane == 0) {
             // ------------------------------------------------ MMA issuer
             bool ok = mbar_wait(bar_q, 0, abort_flag);
-            const uint32_t q_addr = smem_u32(sQ);
+            // Every descriptor the loop uses, computed once: Q's, and K's and V's for both
+            // ring slots.  The MMAs then go out with no arithmetic between them (the
+            // issuing thread shares its SMSP with row warps).
+            constexpr int NS = DP / 16, NV = C / 16;
+            uint64_t qd[NS], kd[2][NS], vd[2][NV];
+            {
+                const uint32_t q_addr = smem_u32(sQ);
+#pragma unroll
+                for (int kk = 0; kk < NS; ++kk) {
+                    qd[kk] = smem_desc(q_addr + (kk >> 2) * S2_QPANEL + (kk & 3) * 32, 16, 1024);
+#pragma unroll
+                    for (int sl = 0; sl < 2; ++sl)
+                        kd[sl][kk] = smem_desc(smem_u32(sK + sl * S2_KV) + (kk >> 2) * S2_KPANEL +
+                                                   (kk & 3) * 32, 16, 1024);
+                }
+#pragma unroll
+                for (int kk = 0; kk < NV; ++kk)
+#pragma unroll
+                    for (int sl = 0; sl < 2; ++sl)
+                        vd[sl][kk] = smem_desc(smem_u32(sV + sl * S2_KV) + kk * 2048, S2_KPANEL, 1024);
+            }
+            auto issue_s = [&](const uint64_t (&kds)[NS], uint32_t s_tmem) {
+#pragma unroll
+                for (int kk = 0; kk < NS; ++kk) mma_f16_ss(s_tmem, qd[kk], kds[kk], IDESC_S, kk > 0 ? 1u : 0u);
+            };
+            // P from tensor memory (8 columns per 16 keys); V: MN-major, 64-column atoms
+            auto issue_pv = [&](const uint64_t (&vds)[NV], uint32_t p_tmem, bool first) {
+#pragma unroll
+                for (int kk = 0; kk < NV; ++kk)
+                    mma_f16_ts(tmem_base + S2_O_COL, p_tmem + kk * 8, vds[kk], IDESC_PV,
+                               (!first || kk > 0) ? 1u : 0u);
+            };
             for (int j = 0; ok && j <= nchunks; ++j) {
                 // step j: K_j (if j < nchunks) and V_{j-1} (if j >= 1) have landed
                 if (!mbar_wait(&kvfull[j & 1], (j >> 1) & 1u, abort_flag)) { ok = false; break; }
@@ -256,34 +287,19 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
                     // S(j) = Q K_j^T into S buffer j & 1 (DP / 16 steps over the head dim).
                     // That buffer held S(j-2), which the row warps read before writing
                     // P(j-2), whose barrier this thread waited for at step j-1.
-                    const uint32_t sk = j % S2_KST;
                     const uint32_t sb = j & 1;
-                    const uint32_t k_addr = smem_u32(sK + sk * S2_KV);
-#pragma unroll
-                    for (int kk = 0; kk < DP / 16; ++kk) {
-                        mma_f16_ss(tmem_base + sb * S2_C,
-                                   smem_desc(q_addr + (kk >> 2) * S2_QPANEL + (kk & 3) * 32, 16, 1024),
-                                   smem_desc(k_addr + (kk >> 2) * S2_KPANEL + (kk & 3) * 32, 16, 1024),
-                                   IDESC_S, kk > 0 ? 1u : 0u);
-                    }
+                    if (j % S2_KST == 0) issue_s(kd[0], tmem_base + sb * S2_C);
+                    else issue_s(kd[1], tmem_base + sb * S2_C);
                     mma_commit(&sfull[sb]);
                 }
                 if (j >= 1) {
                     // O (+)= P_i V_i, i = j - 1 (the rows rescaled O before signalling)
                     const int i = j - 1;
-                    const uint32_t sv = i % S2_VST;
                     if (!mbar_wait(&pfull[i & 1], (i >> 1) & 1u, abort_flag)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t v_addr = smem_u32(sV + sv * S2_KV);
-#pragma unroll
-                    for (int kk = 0; kk < C / 16; ++kk) {
-                        // P from tensor memory (8 columns per 16 keys); V: MN-major,
-                        // 64-column atoms
-                        mma_f16_ts(tmem_base + S2_O_COL,
-                                   tmem_base + S2_P_COL + (i & 1) * (C / 2) + kk * 8,
-                                   smem_desc(v_addr + kk * 2048, S2_KPANEL, 1024), IDESC_PV,
-                                   (i > 0 || kk > 0) ? 1u : 0u);
-                    }
+                    const uint32_t p_tmem = tmem_base + S2_P_COL + (i & 1) * (C / 2);
+                    if (i % S2_VST == 0) issue_pv(vd[0], p_tmem, i == 0);
+                    else issue_pv(vd[1], p_tmem, i == 0);
                     mma_commit(&pvdone[i & 1]);
                 }
             }
