@@ -207,6 +207,10 @@ bi_status encode_tmap_u32(CUtensorMap *map, int rank, void *base, const uint64_t
 //     for decode-shaped calls).  The 256 x 256 pair tile is slower there: each
 //     SM then runs the K loop of a 128 x 256 output, 25 us instead of 20.5 us
 //     at N = 11008, M = 1, and 614 us instead of 589 us over the M = 1..512 sweep.
+//     Wider tiles on one CTA trade the same way: 192 columns take N = 11008,
+//     M = 256 from 37 to 28 us but M = 1 from 20.6 to 23.6 us, and the eleven
+//     batch sizes at N = 11008 and 14336 sum to 602 us (256 columns: 690 us)
+//     against 585 us for 128.
 //   * K = 8192: 256 columns win both for decode-shaped calls and at M = 8192,
 //     and on a CTA pair (256 x 256, a third fewer bytes into each SM) the 8192^3
 //     product runs at 1.81 PFLOP/s, against 1.67 for 128 x 256 on one CTA and
