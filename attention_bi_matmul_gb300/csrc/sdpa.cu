@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
     constexpr int S2_C = C;
     constexpr int HK = C / 2;            // keys per row warp
     constexpr int HD = DP / 2;           // output columns per row warp
-    static_assert(HK == 64 || HK == 32, "P store: 32 or 16 columns per row warp");
+    static_assert(HK == 64 || HK == 32, "row warps hold 32 or 64 keys of a chunk");
     constexpr uint32_t IDESC_S = mma_idesc(IsBf16<T>::value, S2_ROWS, C, false);
     constexpr uint32_t IDESC_PV = mma_idesc(IsBf16<T>::value, S2_ROWS, DP, true);
 
@@ -354,12 +354,16 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
             float x[HK];
             float mloc = -INFINITY;
             if (warp_valid) {
+                // every load of the row's keys in flight before the one wait
 #pragma unroll
                 for (int c32 = 0; c32 < HK / 32; ++c32) {
                     uint32_t(&xu)[32] = *reinterpret_cast<uint32_t(*)[32]>(x + 32 * c32);
                     tmem_ld32(tmem_base + lane_base + sb * S2_C + half * HK + 32 * c32, xu);
-                    tmem_wait_ld(xu);
                 }
+                tmem_wait_ld(*reinterpret_cast<uint32_t(*)[32]>(x));
+#pragma unroll
+                for (int c32 = 1; c32 < HK / 32; ++c32)
+                    tmem_tie(*reinterpret_cast<uint32_t(*)[32]>(x + 32 * c32));
                 if (full) {
 #pragma unroll
                     for (int i = 0; i < HK; i += 2) mloc = fmax3(mloc, x[i], x[i + 1]);
@@ -381,47 +385,56 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
             // operation does): partial sum (key mod 4) k lives in ls01 (k = 0, 1) or
             // ls23 (k = 2, 3) and is added in ascending key order.
             float2 ls01 = make_float2(0.0f, 0.0f), ls23 = make_float2(0.0f, 0.0f);
+            // P_j goes to P buffer j & 1, which held P_{j-2}.  P_{j-2} V_{j-2} is
+            // complete: the MMA thread issued it before S(j), and S(j)'s commit (waited
+            // for above) arrives only once every MMA issued before it has completed.
+            // Keys HK*half.. of row r, two to a 32-bit column (lower key in the low
+            // half), stored 32 keys at a time so that one store is in flight while the
+            // next 32 exponentials are computed.
             if (warp_valid) {
                 const float2 c2 = make_float2(sl2, sl2), nm2 = make_float2(-m_new, -m_new);
+                const uint32_t p_addr = tmem_base + lane_base + S2_P_COL + sb * (C / 2) + half * (HK / 2);
+                auto store32 = [&](int k0) {
+                    uint32_t pw[16];
+#pragma unroll
+                    for (int w = 0; w < 16; ++w) pw[w] = cvt2<T>(x[k0 + 2 * w], x[k0 + 2 * w + 1]);
+                    tmem_st16(p_addr + k0 / 2, pw);
+                };
                 // Two copies of the loop, so that the common (unmasked) one has no
                 // test between the exponentials; both do the same arithmetic.
                 if (full) {
 #pragma unroll
-                    for (int i = 0; i < HK; i += 2) {
-                        const float2 t = __ffma2_rn(make_float2(x[i], x[i + 1]), c2, nm2);
-                        const float e0 = ex2_approx(t.x), e1 = ex2_approx(t.y);
-                        x[i] = e0;
-                        x[i + 1] = e1;
-                        if ((i & 2) == 0) ls01 = __fadd2_rn(ls01, make_float2(e0, e1));
-                        else ls23 = __fadd2_rn(ls23, make_float2(e0, e1));
+                    for (int k0 = 0; k0 < HK; k0 += 32) {
+#pragma unroll
+                        for (int i = k0; i < k0 + 32; i += 2) {
+                            const float2 t = __ffma2_rn(make_float2(x[i], x[i + 1]), c2, nm2);
+                            const float e0 = ex2_approx(t.x), e1 = ex2_approx(t.y);
+                            x[i] = e0;
+                            x[i + 1] = e1;
+                            if ((i & 2) == 0) ls01 = __fadd2_rn(ls01, make_float2(e0, e1));
+                            else ls23 = __fadd2_rn(ls23, make_float2(e0, e1));
+                        }
+                        store32(k0);
                     }
                 } else {
 #pragma unroll
-                    for (int i = 0; i < HK; i += 2) {
-                        const float2 t = __ffma2_rn(make_float2(x[i], x[i + 1]), c2, nm2);
-                        float e0 = ex2_approx(t.x), e1 = ex2_approx(t.y);
-                        if (ARR ? ((vis >> i) & 1u) == 0 : i >= lim) e0 = 0.0f;
-                        if (ARR ? ((vis >> (i + 1)) & 1u) == 0 : i + 1 >= lim) e1 = 0.0f;
-                        x[i] = e0;
-                        x[i + 1] = e1;
-                        if ((i & 2) == 0) ls01 = __fadd2_rn(ls01, make_float2(e0, e1));
-                        else ls23 = __fadd2_rn(ls23, make_float2(e0, e1));
+                    for (int k0 = 0; k0 < HK; k0 += 32) {
+#pragma unroll
+                        for (int i = k0; i < k0 + 32; i += 2) {
+                            const float2 t = __ffma2_rn(make_float2(x[i], x[i + 1]), c2, nm2);
+                            float e0 = ex2_approx(t.x), e1 = ex2_approx(t.y);
+                            if (ARR ? ((vis >> i) & 1u) == 0 : i >= lim) e0 = 0.0f;
+                            if (ARR ? ((vis >> (i + 1)) & 1u) == 0 : i + 1 >= lim) e1 = 0.0f;
+                            x[i] = e0;
+                            x[i + 1] = e1;
+                            if ((i & 2) == 0) ls01 = __fadd2_rn(ls01, make_float2(e0, e1));
+                            else ls23 = __fadd2_rn(ls23, make_float2(e0, e1));
+                        }
+                        store32(k0);
                     }
                 }
             }
             const float lsum = __fadd_rn(__fadd_rn(ls01.x, ls01.y), __fadd_rn(ls23.x, ls23.y));
-            // P_j goes to P buffer j & 1, which held P_{j-2}.  P_{j-2} V_{j-2} is
-            // complete: the MMA thread issued it before S(j), and S(j)'s commit (waited
-            // for above) arrives only once every MMA issued before it has completed.
-            if (warp_valid) {
-                // keys HK*half.. of row r, two to a 32-bit column (lower key in the low half)
-                uint32_t pw[HK / 2];
-#pragma unroll
-                for (int w = 0; w < HK / 2; ++w) pw[w] = cvt2<T>(x[2 * w], x[2 * w + 1]);
-                const uint32_t p_addr = tmem_base + lane_base + S2_P_COL + sb * (C / 2) + half * (HK / 2);
-                if constexpr (HK == 64) tmem_st32(p_addr, pw);
-                else tmem_st16(p_addr, pw);
-            }
             // O *= alpha for this warp's HD columns, after P_{j-1} V_{j-1} is added in
             // (skipped, wait included, when every row has alpha 1)
             if (j >= 1 && warp_valid && __any_sync(0xffffffffu, alpha != 1.0f)) {
