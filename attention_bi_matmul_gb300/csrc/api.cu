@@ -211,6 +211,9 @@ bi_status encode_tmap_u32(CUtensorMap *map, int rank, void *base, const uint64_t
 //     M = 256 from 37 to 28 us but M = 1 from 20.6 to 23.6 us, and the eleven
 //     batch sizes at N = 11008 and 14336 sum to 602 us (256 columns: 690 us)
 //     against 585 us for 128.
+//     256 x 128 pair tiles (half the weight rows per SM) need twice the CTAs,
+//     so decode-shaped calls run two waves: 42 us instead of 21 at N = 11008,
+//     and the sweep over N = 4096, 11008 and 14336 takes 1231 us against 791.
 //   * K = 8192: 256 columns win both for decode-shaped calls and at M = 8192,
 //     and on a CTA pair (256 x 256, a third fewer bytes into each SM) the 8192^3
 //     product runs at 1.81 PFLOP/s, against 1.67 for 128 x 256 on one CTA and

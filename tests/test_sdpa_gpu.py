@@ -168,6 +168,24 @@ def test_decode_full_size_sampled(bi):
     _no_device_error(bi)
 
 
+@pytest.mark.parametrize("B,H,Hkv,L,D", [(4, 32, 8, 4096, 128), (1, 16, 8, 8192, 256)])
+def test_prefill_full_size_sampled(bi, B, H, Hkv, L, D):
+    """Causal prefill at the sizes its throughput is quoted on, in one call: sampled query
+    positions (first, chunk edges, a ragged middle, last) of two batch entries against the
+    oracle, each position with every head."""
+    q, k, v = synth.sdpa_qkv(B, H, Hkv, L, L, D, "bf16", seed=3, device="cuda")
+    o = bi.sdpa(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    qc, kc, vc = q.cpu(), k.cpu(), v.cpu()
+    for b in sorted({0, B - 1}):
+        for p in (0, 127, 128, 1000, L // 2 + 63, L - 1):
+            ref, nrm = oracle.sdpa(qc[b:b + 1, :, p:p + 1], kc[b:b + 1, :, :p + 1], vc[b:b + 1, :, :p + 1],
+                                   causal=True)
+            check_close(o[b:b + 1, :, p:p + 1], ref, nrm, torch.bfloat16,
+                        "prefill B%d L%d D%d b=%d row %d" % (B, L, D, b, p))
+    _no_device_error(bi)
+
+
 @pytest.mark.parametrize("dt", ["bf16", "fp16"])
 def test_growing_scores_move_the_shift(bi, dt):
     """Keys whose scale grows along the sequence, so a row's chunk maxima keep rising far
