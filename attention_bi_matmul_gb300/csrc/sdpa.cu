@@ -36,7 +36,8 @@
 //     and the added zeros leave m, l and the accumulator unchanged, so extra
 //     chunks that a longer query tile visits, or keys appended beyond a token,
 //     change none of its bits;
-//   * o = acc / l (IEEE division), rounded once to the output dtype;
+//   * o = acc * (1 / l) (the reciprocal correctly rounded, then one fp32 multiply),
+//     rounded once to the output dtype;
 //   * an attention sink (one extra logit per head, no value) enters as the
 //     initial state m = sink * log2 e, l = 1.
 // Head dims that are not a multiple of 64 are loaded with the copy engine's zero
@@ -462,9 +463,10 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
                 m_run = m_new;
             }
         }
-        // the last P V, then o = acc / l
+        // the last P V, then o = acc * (1 / l): one correctly rounded reciprocal per row
         warp_wait(&pvdone[(nchunks - 1) & 1], ((nchunks - 1) >> 1) & 1u, abort_flag);
         tc_fence_after();
+        const float inv_l = __frcp_rn(l_run);
         if (warp_valid) {
             T *orow = static_cast<T *>(args.o) + b * args.os[0] + h * args.os[1] +
                       (pos - q_offset) * args.os[2] + half * HD;
@@ -481,7 +483,7 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
                         float v[8];
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
-                            v[e] = __fdiv_rn(__uint_as_float(ov[d8 * 8 + e]), l_run);
+                            v[e] = __fmul_rn(__uint_as_float(ov[d8 * 8 + e]), inv_l);
                         *reinterpret_cast<uint4 *>(orow + c4 * 32 + d8 * 8) = pack8<T>(v);
                     }
                 }
