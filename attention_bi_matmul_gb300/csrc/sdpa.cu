@@ -168,6 +168,12 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
                                        : static_cast<int>((Lkv + S2_C - 1) / S2_C);
 
     if (threadIdx.x == 0) {
+        // Thread 0 is also the copy producer: the copy descriptors are fetched and the
+        // block's first copies (Q, and K_0 for step 0) go out before the rest of the
+        // block's setup, so that their latency overlaps it.
+        prefetch_tmap(&tmQ);
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
         mbar_init(bar_q, 1);
         for (int s = 0; s < 2; ++s) mbar_init(&kvfull[s], 1);
         for (int i = 0; i < 2; ++i) {
@@ -180,6 +186,16 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
         mbar_init(mma_done, 1);
         *abort_flag = 0;
         fence_barrier_init();
+        const int32_t qi0 = static_cast<int32_t>(p_lo - q_offset);  // may be negative
+        mbar_arrive_expect_tx(bar_q, S2Smem::QB);
+#pragma unroll
+        for (uint32_t pn = 0; pn < NP; ++pn)
+            tma_load_4d(sQ + pn * S2_QPANEL, &tmQ, bar_q, 64 * pn, kvh * G, qi0, b);
+        // step 0 of the loop below: K_0 alone (nchunks >= 1), into K slot 0
+        mbar_arrive_expect_tx(&kvfull[0], S2_KV);
+#pragma unroll
+        for (uint32_t pn = 0; pn < NP; ++pn)
+            tma_load_4d(sK + pn * S2_KPANEL, &tmK, &kvfull[0], 64 * pn, 0, kvh, b);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, S2_TMEM_COLS);
@@ -193,25 +209,18 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
-            prefetch_tmap(&tmQ);
-            prefetch_tmap(&tmK);
-            prefetch_tmap(&tmV);
-            const int32_t qi0 = static_cast<int32_t>(p_lo - q_offset);  // may be negative
-            mbar_arrive_expect_tx(bar_q, S2Smem::QB);
-#pragma unroll
-            for (uint32_t pn = 0; pn < NP; ++pn)
-                tma_load_4d(sQ + pn * S2_QPANEL, &tmQ, bar_q, 64 * pn, kvh * G, qi0, b);
-            // Step j loads K_j and V_{j-1} onto one barrier, so that the MMA thread
-            // waits once per chunk for both (each wait costs the tensor pipe time).
+            // Q and step 0 were issued during the block's setup.  Step j loads K_j and
+            // V_{j-1} onto one barrier, so that the MMA thread waits once per chunk for
+            // both (each wait costs the tensor pipe time).
             // Every step, the last one (V only) included, first waits for S(j-2)
             // (K slot j % 2 read): the MMA thread issues S(j-2) only after its wait
             // on step j-2, which used this same barrier, so the barrier is never
             // armed again before that phase has been consumed.  The V slot waits for
             // P_{j-3} V_{j-3}.  Both are the MMA's own completion barriers, so it
             // commits twice per chunk, not four times.
-            int armed = 0;
+            int armed = 1;
             bool ok = true;
-            for (int j = 0; j <= nchunks; ++j) {
+            for (int j = 1; j <= nchunks; ++j) {
                 const bool has_k = j < nchunks, has_v = j >= 1;
                 if (!mbar_wait(&sfull[j & 1], ((j >> 1) & 1u) ^ 1u, abort_flag)) {
                     ok = false;
