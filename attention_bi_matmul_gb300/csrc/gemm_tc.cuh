@@ -198,8 +198,50 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int64_t total = args.batch * num_m * num_n;
     const int KB = static_cast<int>((K + KP * TC_BK - 1) / (KP * TC_BK));   // stages per tile
 
+    // The producer's copies.  The A copy moves only the rows that exist (a_rows <= 128);
+    // tile rows past them are never stored, and no row's result depends on another row.
+    const uint32_t tx = KP * (static_cast<uint32_t>(args.a_rows) * TC_BK * 2 + B_PANEL);
+    // ring stage s <- K panels kb * KP.. of tile (mb, nb) of batch entries (ea, eb)
+    auto copy_stage = [&](uint32_t s, int kb, int64_t mb, int64_t nb, int32_t ea, int32_t eb) {
+        mbar_arrive_expect_tx(&full[s], tx);
+#pragma unroll
+        for (int p = 0; p < KP; ++p) {
+            const int32_t k0 = (kb * KP + p) * TC_BK;   // beyond K: zero-filled
+            tma_load_3d(sA + s * A_BYTES + p * A_PANEL, &tmA, &full[s], k0,
+                        static_cast<int32_t>(mb * TC_BM), ea);
+            if (!B_MN) {
+                tma_load_3d(sB + s * B_BYTES + p * B_PANEL, &tmB, &full[s], k0,
+                            static_cast<int32_t>(nb * BN), eb);
+            } else {
+#pragma unroll
+                for (int j = 0; j < BN / 64; ++j)
+                    tma_load_3d(sB + s * B_BYTES + p * B_PANEL + j * 8192, &tmB, &full[s],
+                                static_cast<int32_t>(nb * BN + j * 64), k0, eb);
+            }
+        }
+    };
+    // 128-column tiles stream their weight panels from HBM; the producer asks for the
+    // panels one ring further on to move into L2 as it copies a stage.  (Measured: +2-5%
+    // for those; it costs the L2-resident 256-wide tiles 7%, so they do not.
+    // Prefetching further ahead was slower.)
+    auto prefetch_stage = [&](int kq_stage, int64_t nb, int32_t eb) {
+#pragma unroll
+        for (int p = 0; p < KP; ++p) {
+            const int32_t kq = (kq_stage * KP + p) * TC_BK;
+            if (!B_MN) {
+                tma_prefetch_3d(&tmB, kq, static_cast<int32_t>(nb * BN), eb);
+            } else {
+#pragma unroll
+                for (int j = 0; j < BN / 64; ++j)
+                    tma_prefetch_3d(&tmB, static_cast<int32_t>(nb * BN + j * 64), kq, eb);
+            }
+        }
+    };
+
     if (threadIdx.x == 0) {
-        // fetch the copy descriptors while the block sets up (the first copy waits for them)
+        // Thread 0 is also the copy producer: it fetches the copy descriptors and sends
+        // the block's first stage before the TMEM allocation and the block barrier, so
+        // that the copy's latency overlaps the setup (the grid never exceeds the tiles).
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
         for (int s = 0; s < STAGES; ++s) {
@@ -213,6 +255,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         mbar_init(mma_done, 1);
         *abort_flag = 0;
         fence_barrier_init();
+        int64_t e, mb, nb;
+        tc_tile_coords(blockIdx.x, num_m, num_n, e, mb, nb);
+        const int32_t eb = args.sb ? static_cast<int32_t>(e) : 0;
+        copy_stage(0, 0, mb, nb, args.sa ? static_cast<int32_t>(e) : 0, eb);
+        if (tc_l2_prefetch<BN>() && STAGES < KB) prefetch_stage(STAGES, nb, eb);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, TMEM_COLS);
@@ -226,53 +273,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
-            // The A copy moves only the rows that exist (a_rows <= 128); tile rows past
-            // them are never stored, and no row's result depends on another row.
-            const uint32_t tx = KP * (static_cast<uint32_t>(args.a_rows) * TC_BK * 2 + B_PANEL);
-            uint32_t it = 0, s = 0, ph = 0;
+            // Stage 0 of the first tile went out during the setup.
+            uint32_t it = 1, s = 1, ph = 0;
+            if (s == static_cast<uint32_t>(STAGES)) { s = 0; ph = 1u; }
             bool ok = true;
-            auto prefetch_stage = [&](int kq_stage, int64_t nb, int32_t eb) {
-#pragma unroll
-                for (int p = 0; p < KP; ++p) {
-                    const int32_t kq = (kq_stage * KP + p) * TC_BK;
-                    if (!B_MN) {
-                        tma_prefetch_3d(&tmB, kq, static_cast<int32_t>(nb * BN), eb);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < BN / 64; ++j)
-                            tma_prefetch_3d(&tmB, static_cast<int32_t>(nb * BN + j * 64), kq, eb);
-                    }
-                }
-            };
             for (int64_t t = blockIdx.x; ok && t < total; t += gridDim.x) {
                 int64_t e, mb, nb;
                 tc_tile_coords(t, num_m, num_n, e, mb, nb);
                 // A shared operand is a tensor map with one batch entry.
                 const int32_t ea = args.sa ? static_cast<int32_t>(e) : 0;
                 const int32_t eb = args.sb ? static_cast<int32_t>(e) : 0;
-                for (int kb = 0; kb < KB; ++kb, ++it) {
+                for (int kb = t == blockIdx.x ? 1 : 0; kb < KB; ++kb, ++it) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&full[s], tx);
-#pragma unroll
-                    for (int p = 0; p < KP; ++p) {
-                        const int32_t k0 = (kb * KP + p) * TC_BK;   // beyond K: zero-filled
-                        tma_load_3d(sA + s * A_BYTES + p * A_PANEL, &tmA, &full[s], k0,
-                                    static_cast<int32_t>(mb * TC_BM), ea);
-                        if (!B_MN) {
-                            tma_load_3d(sB + s * B_BYTES + p * B_PANEL, &tmB, &full[s], k0,
-                                        static_cast<int32_t>(nb * BN), eb);
-                        } else {
-#pragma unroll
-                            for (int j = 0; j < BN / 64; ++j)
-                                tma_load_3d(sB + s * B_BYTES + p * B_PANEL + j * 8192, &tmB,
-                                            &full[s], static_cast<int32_t>(nb * BN + j * 64), k0,
-                                            eb);
-                        }
-                    }
-                    // 128-column tiles stream their weight panels from HBM; ask for the
-                    // panels one ring further on to move into L2 now.  (Measured: +2-5%
-                    // for those; it costs the L2-resident 256-wide tiles 7%, so they do
-                    // not.  Prefetching further ahead was slower.)
+                    copy_stage(s, kb, mb, nb, ea, eb);
                     if (tc_l2_prefetch<BN>() && kb + STAGES < KB) prefetch_stage(kb + STAGES, nb, eb);
                     if (++s == STAGES) { s = 0; ph ^= 1u; }
                 }
