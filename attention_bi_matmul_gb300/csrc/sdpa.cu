@@ -256,10 +256,9 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------------ MMA issuer
-            bool ok = mbar_wait(bar_q, 0, abort_flag);
-            // Every descriptor the loop uses, computed once: Q's, and K's and V's for both
-            // ring slots.  The MMAs then go out with no arithmetic between them (the
-            // issuing thread shares its SMSP with row warps).
+            // Every descriptor the loop uses, computed once (before Q has landed): Q's,
+            // and K's and V's for both ring slots.  The MMAs then go out with no
+            // arithmetic between them (the issuing thread shares its SMSP with row warps).
             constexpr int NS = DP / 16, NV = C / 16;
             uint64_t qd[NS], kd[2][NS], vd[2][NV];
             {
@@ -278,6 +277,7 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
                     for (int sl = 0; sl < 2; ++sl)
                         vd[sl][kk] = smem_desc(smem_u32(sV + sl * S2_KV) + kk * 2048, S2_KPANEL, 1024);
             }
+            bool ok = mbar_wait(bar_q, 0, abort_flag);
             auto issue_s = [&](const uint64_t (&kds)[NS], uint32_t s_tmem) {
 #pragma unroll
                 for (int kk = 0; kk < NS; ++kk) mma_f16_ss(s_tmem, qd[kk], kds[kk], IDESC_S, kk > 0 ? 1u : 0u);
@@ -479,22 +479,30 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
         if (warp_valid) {
             T *orow = static_cast<T *>(args.o) + b * args.os[0] + h * args.os[1] +
                       (pos - q_offset) * args.os[2] + half * HD;
+            // two 32-column loads in flight per wait
+            constexpr int OB = HD / 32 < 2 ? HD / 32 : 2;
 #pragma unroll 1
-            for (int c4 = 0; c4 < HD / 32; ++c4) {
-                uint32_t ov[32];
-                tmem_ld32(o_addr + c4 * 32, ov);
-                tmem_wait_ld(ov);
+            for (int c0 = 0; c0 < HD / 32; c0 += OB) {
+                uint32_t ov[OB][32];
+#pragma unroll
+                for (int u = 0; u < OB; ++u) tmem_ld32(o_addr + (c0 + u) * 32, ov[u]);
+                tmem_wait_ld(ov[0]);
+#pragma unroll
+                for (int u = 1; u < OB; ++u) tmem_tie(ov[u]);
                 if (valid && !*abort_flag) {
 #pragma unroll
-                    for (int d8 = 0; d8 < 4; ++d8) {
-                        const int col = half * HD + c4 * 32 + d8 * 8;
-                        if (col >= args.D) break;        // padded columns past the head dim
-                        float v[8];
+                    for (int u = 0; u < OB; ++u)
 #pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            v[e] = __fmul_rn(__uint_as_float(ov[d8 * 8 + e]), inv_l);
-                        *reinterpret_cast<uint4 *>(orow + c4 * 32 + d8 * 8) = pack8<T>(v);
-                    }
+                        for (int d8 = 0; d8 < 4; ++d8) {
+                            const int c4 = c0 + u;
+                            const int col = half * HD + c4 * 32 + d8 * 8;
+                            if (col >= args.D) break;        // padded columns past the head dim
+                            float v[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                v[e] = __fmul_rn(__uint_as_float(ov[u][d8 * 8 + e]), inv_l);
+                            *reinterpret_cast<uint4 *>(orow + c4 * 32 + d8 * 8) = pack8<T>(v);
+                        }
                 }
             }
         }
