@@ -10,6 +10,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstring>
+#include <mutex>
 
 #include <cudaTypedefs.h>
 
@@ -26,10 +27,15 @@ namespace {
 
 std::atomic<int64_t> g_launches{0};
 
+// Per-device state, filled once under g_init_mutex and published by the release store
+// of g_ready[dev]; entry points called from several host threads read it after the
+// acquire load in check_device.
 constexpr int MAX_DEV = 64;
-uint32_t *g_err_ptr[MAX_DEV] = {};
-int g_sm_count[MAX_DEV] = {};
-int g_arch_ok[MAX_DEV] = {};  // 0 unknown, 1 sm_103, -1 other
+std::mutex g_init_mutex;
+std::atomic<uint32_t *> g_err_ptr[MAX_DEV] = {};
+std::atomic<int> g_sm_count[MAX_DEV] = {};
+std::atomic<int> g_arch_ok[MAX_DEV] = {};  // 0 unknown, 1 sm_103, -1 other
+std::atomic<int> g_ready[MAX_DEV] = {};    // per-device initialisation done
 
 int current_device() {
     int dev = 0;
@@ -37,48 +43,57 @@ int current_device() {
     return (dev >= 0 && dev < MAX_DEV) ? dev : -1;
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::atomic<PFN_cuTensorMapEncodeTiled_v12000> g_encode{nullptr};
 
-bool load_encode() {
-    if (g_encode) return true;
+// The driver's tensor-map encoder (the same function for every device).  Two threads
+// may both look it up; they store the same pointer.
+PFN_cuTensorMapEncodeTiled_v12000 load_encode() {
+    PFN_cuTensorMapEncodeTiled_v12000 f = g_encode.load(std::memory_order_acquire);
+    if (f) return f;
     void *fn = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
                                          &q) != cudaSuccess ||
         q != cudaDriverEntryPointSuccess || !fn)
-        return false;
-    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    return true;
+        return nullptr;
+    f = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    g_encode.store(f, std::memory_order_release);
+    return f;
 }
-
-int g_ready[MAX_DEV] = {};     // per-device initialisation done
 
 bi_status device_init(int dev);
 
 // The code in this library is built for sm_103a only.  The first call on a
 // device also initialises everything later calls need on it (see device_init),
-// so that no later call makes a non-stream CUDA call.
+// so that no later call makes a non-stream CUDA call.  Concurrent first calls
+// from several host threads are serialised; later calls take no lock.
 bi_status check_device() {
     const int dev = current_device();
     if (dev < 0) return BI_ERR_CUDA;
-    if (g_arch_ok[dev] == 0) {
+    if (g_ready[dev].load(std::memory_order_acquire)) return BI_OK;
+    std::lock_guard<std::mutex> lock(g_init_mutex);
+    if (g_ready[dev].load(std::memory_order_relaxed)) return BI_OK;
+    if (g_arch_ok[dev].load(std::memory_order_relaxed) == 0) {
         int major = 0, minor = 0;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
             return BI_ERR_CUDA;
-        g_arch_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+        g_arch_ok[dev].store((major == 10 && minor == 3) ? 1 : -1, std::memory_order_relaxed);
     }
-    if (g_arch_ok[dev] != 1) return BI_ERR_UNSUPPORTED;
-    if (!g_ready[dev]) {
-        bi_status st = device_init(dev);
-        if (st != BI_OK) return st;
-        g_ready[dev] = 1;
-    }
+    if (g_arch_ok[dev].load(std::memory_order_relaxed) != 1) return BI_ERR_UNSUPPORTED;
+    bi_status st = device_init(dev);
+    if (st != BI_OK) return st;
+    g_ready[dev].store(1, std::memory_order_release);
     return BI_OK;
 }
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool valid_dtype(bi_dtype dt) { return dt == BI_F32 || dt == BI_F16 || dt == BI_BF16; }
+// Element alignment of a pointer that kernels read or write one element at a time
+// (2 bytes for the 16-bit dtypes, 4 for fp32); null passes.
+inline bool elem_aligned(const void *p, bi_dtype dt) {
+    return (reinterpret_cast<uintptr_t>(p) & (dt == BI_F32 ? 3u : 1u)) == 0;
+}
 
 // Common validation of the GEMM family.  Returns BI_OK to proceed.
 bi_status check_gemm(const void *a, int64_t lda, const void *b, int64_t ldb, void *y, int64_t ldy,
@@ -137,28 +152,32 @@ void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 uint32_t *device_error_word() {
     const int dev = current_device();
     if (dev < 0) return nullptr;
-    if (!g_err_ptr[dev]) {
+    uint32_t *w = g_err_ptr[dev].load(std::memory_order_acquire);
+    if (!w) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
-        g_err_ptr[dev] = static_cast<uint32_t *>(p);
+        w = static_cast<uint32_t *>(p);
+        g_err_ptr[dev].store(w, std::memory_order_release);
     }
-    return g_err_ptr[dev];
+    return w;
 }
 
 int device_sm_count() {
     const int dev = current_device();
     if (dev < 0) return 1;
-    if (!g_sm_count[dev]) {
-        int n = 0;
+    int n = g_sm_count[dev].load(std::memory_order_acquire);
+    if (!n) {
         cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        g_sm_count[dev] = n > 0 ? n : 1;
+        n = n > 0 ? n : 1;
+        g_sm_count[dev].store(n, std::memory_order_release);
     }
-    return g_sm_count[dev];
+    return n;
 }
 
 bi_status encode_tmap(CUtensorMap *map, bi_dtype dt, int rank, void *base, const uint64_t *dims,
                       const uint64_t *strides_bytes, const uint32_t *box, bool swizzle128) {
-    if (!load_encode()) return BI_ERR_CUDA;
+    const PFN_cuTensorMapEncodeTiled_v12000 encode = load_encode();
+    if (!encode) return BI_ERR_CUDA;
     const CUtensorMapDataType t = dt == BI_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                   : dt == BI_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
@@ -170,7 +189,7 @@ bi_status encode_tmap(CUtensorMap *map, bi_dtype dt, int rank, void *base, const
         estr[i] = 1;
     }
     for (int i = 0; i + 1 < rank; ++i) gstr[i] = strides_bytes[i];
-    const CUresult r = g_encode(map, t, static_cast<cuuint32_t>(rank), base, gdim, gstr, bdim, estr,
+    const CUresult r = encode(map, t, static_cast<cuuint32_t>(rank), base, gdim, gstr, bdim, estr,
                                 CU_TENSOR_MAP_INTERLEAVE_NONE,
                                 swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -182,7 +201,8 @@ bi_status encode_tmap(CUtensorMap *map, bi_dtype dt, int rank, void *base, const
 // rows are stored with the 128-byte swizzle (16-byte chunk c of row r at c ^ (r % 8)).
 bi_status encode_tmap_u32(CUtensorMap *map, int rank, void *base, const uint64_t *dims,
                           const uint64_t *strides_bytes, const uint32_t *box, bool swizzle128) {
-    if (!load_encode()) return BI_ERR_CUDA;
+    const PFN_cuTensorMapEncodeTiled_v12000 encode = load_encode();
+    if (!encode) return BI_ERR_CUDA;
     cuuint64_t gdim[5], gstr[4];
     cuuint32_t bdim[5], estr[5];
     for (int i = 0; i < rank; ++i) {
@@ -191,7 +211,7 @@ bi_status encode_tmap_u32(CUtensorMap *map, int rank, void *base, const uint64_t
         estr[i] = 1;
     }
     for (int i = 0; i + 1 < rank; ++i) gstr[i] = strides_bytes[i];
-    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, static_cast<cuuint32_t>(rank),
+    const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, static_cast<cuuint32_t>(rank),
                                 base, gdim, gstr, bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                                 swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -277,6 +297,7 @@ bi_status bi_linear(const void *x, int64_t ldx, const void *w, int64_t ldw, cons
                     bi_stream_t stream) {
     bi_status st = check_gemm(x, ldx, w, ldw, y, ldy, M, N, K, dtype, true);
     if (st != BI_OK) return st;
+    if (!elem_aligned(bias, dtype)) return BI_ERR_ALIGNMENT;   // read one element at a time
     GemmArgs args{};
     args.M = M; args.N = N; args.K = K; args.y = y; args.ldy = ldy; args.batch = 1;
     args.bias = bias;
@@ -355,6 +376,7 @@ bi_status bi_addmm(const void *c, int64_t ldc, const void *a, int64_t lda, const
     if (st != BI_OK) return st;
     if (!c || ldc < 0 || (ldc > 0 && ldc < N)) return BI_ERR_INVALID_ARG;
     if (!std::isfinite(alpha) || !std::isfinite(beta)) return BI_ERR_INVALID_ARG;
+    if (!elem_aligned(c, dtype)) return BI_ERR_ALIGNMENT;      // read one element at a time
     GemmArgs args{};
     args.M = M; args.N = N; args.K = K; args.y = y; args.ldy = ldy; args.batch = 1;
     args.c = c; args.ldc = ldc; args.alpha = alpha; args.beta = beta;
@@ -478,6 +500,8 @@ bi_status bi_rmsnorm(const void *x, int64_t ldx, const void *w, void *y, int64_t
     if (!valid_dtype(dtype)) return BI_ERR_UNSUPPORTED;
     if (!x || !w || !y || M < 0 || N <= 0 || ldx < N || ldy < N) return BI_ERR_INVALID_ARG;
     if (!(eps >= 0.0f) || !std::isfinite(eps)) return BI_ERR_INVALID_ARG;
+    if (!elem_aligned(x, dtype) || !elem_aligned(w, dtype) || !elem_aligned(y, dtype))
+        return BI_ERR_ALIGNMENT;
     if (M == 0) return BI_OK;
     bi_status st = check_device();
     if (st != BI_OK) return st;
@@ -492,6 +516,7 @@ bi_status bi_rope(const void *x, const int64_t xs[4], void *y, const int64_t ys[
         return BI_ERR_INVALID_ARG;
     if (!(base > 1.0f) || !std::isfinite(base)) return BI_ERR_INVALID_ARG;
     if (xs[3] != 1 || ys[3] != 1) return BI_ERR_INVALID_ARG;
+    if (!elem_aligned(x, dtype) || !elem_aligned(y, dtype)) return BI_ERR_ALIGNMENT;
     if (B == 0 || L == 0) return BI_OK;
     bi_status st = check_device();
     if (st != BI_OK) return st;
@@ -503,6 +528,7 @@ bi_status bi_swiglu(const void *gu, int64_t ldgu, void *y, int64_t ldy, int64_t 
                     bi_dtype dtype, bi_stream_t stream) {
     if (!valid_dtype(dtype)) return BI_ERR_UNSUPPORTED;
     if (!gu || !y || M < 0 || I <= 0 || ldgu < 2 * I || ldy < I) return BI_ERR_INVALID_ARG;
+    if (!elem_aligned(gu, dtype) || !elem_aligned(y, dtype)) return BI_ERR_ALIGNMENT;
     if (M == 0) return BI_OK;
     bi_status st = check_device();
     if (st != BI_OK) return st;
@@ -513,6 +539,8 @@ bi_status bi_add(const void *a, const void *b, void *y, int64_t n, bi_dtype dtyp
                  bi_stream_t stream) {
     if (!valid_dtype(dtype)) return BI_ERR_UNSUPPORTED;
     if (!a || !b || !y || n < 0) return BI_ERR_INVALID_ARG;
+    if (!elem_aligned(a, dtype) || !elem_aligned(b, dtype) || !elem_aligned(y, dtype))
+        return BI_ERR_ALIGNMENT;
     if (n == 0) return BI_OK;
     bi_status st = check_device();
     if (st != BI_OK) return st;
@@ -525,6 +553,8 @@ bi_status bi_embedding(const int64_t *ids, int64_t n_ids, const void *table, int
     if (!valid_dtype(dtype)) return BI_ERR_UNSUPPORTED;
     if (!ids || !table || !y || n_ids < 0 || vocab <= 0 || dim <= 0 || ldt < dim || ldy < dim)
         return BI_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(ids) & 7u) return BI_ERR_ALIGNMENT;   // read as int64
+    if (n_ids > 0x7fffffff) return BI_ERR_UNSUPPORTED;                     // one block per id
     if (n_ids == 0) return BI_OK;
     bi_status st = check_device();
     if (st != BI_OK) return st;
@@ -540,6 +570,7 @@ bi_status bi_copy4d(const void *src, const int64_t ss[4], void *dst, const int64
     for (int i = 0; i < 4; ++i)
         if (n[i] < 0 || ss[i] < 0 || ds[i] < 0) return BI_ERR_INVALID_ARG;
     if (ss[3] != 1 || ds[3] != 1) return BI_ERR_INVALID_ARG;
+    if (!elem_aligned(src, dtype) || !elem_aligned(dst, dtype)) return BI_ERR_ALIGNMENT;
     if (n[0] * n[1] * n[2] * n[3] == 0) return BI_OK;
     bi_status st = check_device();
     if (st != BI_OK) return st;

@@ -66,15 +66,18 @@ class Decoder:
                  torch.zeros(shape, dtype=self.dtype, device=self.device))
                 for _ in range(c.n_layers)]
 
-    def forward(self, ids: torch.Tensor, cache, pos0: int) -> torch.Tensor:
+    def forward(self, ids: torch.Tensor, cache, pos0: int, trace: dict | None = None) -> torch.Tensor:
         """ids[B, L] at absolute positions pos0 .. pos0+L-1 -> logits[B, L, vocab].
 
-        Writes the new keys/values into ``cache`` at those positions."""
+        Writes the new keys/values into ``cache`` at those positions.  With ``trace``
+        (a dict), every intermediate tensor is also stored there under "<layer>.<name>"
+        (layer "f" for the final norm and LM head), so that each op can be checked on
+        its own inputs; nothing else changes."""
         c = self.cfg
         B, L = ids.shape
         T = B * L
         h = bi.embedding(ids.reshape(-1).contiguous(), self.emb)            # [T, d]
-        for lw, (kc, vc) in zip(self.layers, cache):
+        for i, (lw, (kc, vc)) in enumerate(zip(self.layers, cache)):
             n = bi.rmsnorm(h, lw["ln1"], c.eps)
             qkv = bi.linear(n, lw["wqkv"]).view(B, L, c.H + 2 * c.Hkv, c.D)
             q = bi.rope(qkv[:, :, :c.H], pos0, c.rope_base)                 # [B, L, H, D]
@@ -85,11 +88,23 @@ class Decoder:
             bi.sdpa(q.transpose(1, 2), kc[:, :, :pos0 + L], vc[:, :, :pos0 + L], causal=True,
                     q_offset=pos0, out=att.transpose(1, 2))
             o = bi.linear(att.view(T, c.H * c.D), lw["wo"])
-            h = bi.add(h, o)
-            n = bi.rmsnorm(h, lw["ln2"], c.eps)
-            a = bi.swiglu(bi.linear(n, lw["wgu"]))
-            h = bi.add(h, bi.linear(a, lw["wdown"]))
+            h1 = bi.add(h, o)
+            n2 = bi.rmsnorm(h1, lw["ln2"], c.eps)
+            gu = bi.linear(n2, lw["wgu"])
+            a = bi.swiglu(gu)
+            down = bi.linear(a, lw["wdown"])
+            h2 = bi.add(h1, down)
+            if trace is not None:
+                for name, t in (("h_in", h), ("n1", n), ("qkv", qkv), ("q", q),
+                                ("k_cache", kc[:, :, :pos0 + L]), ("v_cache", vc[:, :, :pos0 + L]),
+                                ("att", att), ("o", o), ("h1", h1), ("n2", n2), ("gu", gu),
+                                ("a", a), ("down", down), ("h_out", h2)):
+                    trace["%d.%s" % (i, name)] = t.clone()
+            h = h2
         n = bi.rmsnorm(h, self.lnf, c.eps)
-        return bi.linear(n, self.lm_head).view(B, L, c.vocab)
+        logits = bi.linear(n, self.lm_head).view(B, L, c.vocab)
+        if trace is not None:
+            trace.update({"f.h_in": h, "f.n": n, "f.logits": logits})
+        return logits
 
     __call__ = forward

@@ -7,13 +7,19 @@
  *     nothing and returns a non-zero bi_status;
  *   - allocates nothing, synchronises nothing and launches on `stream` only
  *     (so the same call is legal inside CUDA-graph capture);
- *   - chooses its kernel and tile configuration from (dtype, N, K, weight
- *     layout) for GEMMs and (dtype, head_dim, group size, mask) for attention,
- *     never from M, the batch, the query length, the context length or a
- *     pointer value.  That is the batch-invariance contract: the bits of one
+ *   - chooses its kernel, tile shape and reduction order from (dtype, N, K,
+ *     weight layout) for GEMMs and (dtype, head_dim, group size, mask) for
+ *     attention, never from M, the batch, the query length, the context length
+ *     or a pointer value.  That is the batch-invariance contract: the bits of one
  *     output row do not depend on batch size, batch neighbours, query length
  *     (decode vs chunked prefill), KV-cache length, or eager vs graph replay
  *     ("mlx-batch-invariant" README, "What batch-invariant means here").
+ *     Some scheduling does follow M, and none of it changes which products are
+ *     summed or in what order: the number of A rows each tensor-memory copy
+ *     moves (M rounded up to 16, at most one tile), the shared-memory ring depth
+ *     that those smaller copies leave room for, the GEMM pair kernel's one or two
+ *     K panels per ring stage (two when every CTA pair has at least two tiles),
+ *     and the grid size (never more blocks than tiles).
  *
  * Layout: row-major, the last dimension contiguous.  Leading dimensions (ld*)
  * and strides are in ELEMENTS.  dtypes: BI_F32, BI_F16, BI_BF16 -- all

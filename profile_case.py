@@ -1,12 +1,12 @@
 """Run one kernel case a few times, for profilers (ncu) and quick timing.
 
-  python -m attention_bi_matmul_gb300.profile_case linear M N K [--reps R]
-  python -m attention_bi_matmul_gb300.profile_case matmul M N K [--reps R]
-  python -m attention_bi_matmul_gb300.profile_case sdpa B H Hkv Lq Lkv [--reps R]
-  python -m attention_bi_matmul_gb300.profile_case qlinear M N K BITS GROUP [--reps R]
+  python profile_case.py linear M N K [--reps R]
+  python profile_case.py matmul M N K [--reps R]
+  python profile_case.py sdpa B H Hkv Lq Lkv [--reps R]
+  python profile_case.py qlinear M N K BITS GROUP [--reps R]
       (bf16 activations; each call on one of 8 quantized weight copies, so the
       packed weights come from HBM)
-  python -m attention_bi_matmul_gb300.profile_case sweep [--reps R]
+  python profile_case.py sweep [--reps R]
       (bf16 linear, K=4096, N in {4096, 11008, 14336}, M in {1,..,512}, each call
       on one of 4 weight copies, as in the benchmark's batch sweep)
 
@@ -22,7 +22,7 @@ import sys
 
 import torch
 
-ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 

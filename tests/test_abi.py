@@ -180,3 +180,35 @@ def test_glue_validation(lib):
     assert lib.bi_add(p, p, p, -1, L.BI_BF16, s) == L.BI_ERR_INVALID_ARG
     assert lib.bi_debug_wait_probe(0, s) == L.BI_ERR_INVALID_ARG
     assert lib.bi_debug_wait_probe(3000000, s) == L.BI_ERR_INVALID_ARG
+
+
+def test_element_alignment_of_per_element_operands(lib):
+    """Pointers the kernels read or write one element at a time (the bias, addmm's c, the
+    glue ops' tensors) must be aligned to their element size, and the embedding ids to 8
+    bytes; a misaligned one is refused on the host, before any launch."""
+    p = ctypes.c_void_p(4096)
+    odd = ctypes.c_void_p(4096 + 1)          # misaligned for 16-bit elements
+    half = ctypes.c_void_p(4096 + 2)         # 2-byte aligned: fine for 16-bit, not for fp32
+    s = ctypes.c_void_p(0)
+    # bias of bi_linear
+    assert lib.bi_linear(p, 16, p, 16, odd, p, 16, 2, 16, 16, L.BI_BF16, s) == L.BI_ERR_ALIGNMENT
+    assert lib.bi_linear(p, 16, p, 16, half, p, 16, 2, 16, 16, L.BI_F32, s) == L.BI_ERR_ALIGNMENT
+    # c of bi_addmm, full and broadcast row
+    for ldc in (16, 0):
+        assert lib.bi_addmm(odd, ldc, p, 16, p, 16, p, 16, 2, 16, 16, 1.0, 1.0, L.BI_F16, s) \
+            == L.BI_ERR_ALIGNMENT
+        assert lib.bi_addmm(half, ldc, p, 16, p, 16, p, 16, 2, 16, 16, 1.0, 1.0, L.BI_F32, s) \
+            == L.BI_ERR_ALIGNMENT
+    # glue ops
+    assert lib.bi_rmsnorm(odd, 16, p, p, 16, 1, 16, 1e-6, L.BI_BF16, s) == L.BI_ERR_ALIGNMENT
+    assert lib.bi_rmsnorm(p, 16, half, p, 16, 1, 16, 1e-6, L.BI_F32, s) == L.BI_ERR_ALIGNMENT
+    assert lib.bi_swiglu(p, 16, odd, 8, 1, 8, L.BI_BF16, s) == L.BI_ERR_ALIGNMENT
+    assert lib.bi_add(p, odd, p, 4, L.BI_F16, s) == L.BI_ERR_ALIGNMENT
+    x4 = L.i64arr([1024, 256, 128, 1])
+    assert lib.bi_rope(odd, x4, p, x4, 1, 2, 2, 128, 0, 1e4, L.BI_BF16, s) == L.BI_ERR_ALIGNMENT
+    n4 = L.i64arr([1, 1, 1, 4])
+    assert lib.bi_copy4d(p, x4, odd, x4, n4, L.BI_BF16, s) == L.BI_ERR_ALIGNMENT
+    # embedding: int64 ids 8-byte aligned; at most 2^31 - 1 ids (one block each)
+    assert lib.bi_embedding(ctypes.c_void_p(4096 + 4), 4, p, 8, 10, p, 8, 8, L.BI_BF16, s) \
+        == L.BI_ERR_ALIGNMENT
+    assert lib.bi_embedding(p, 1 << 31, p, 8, 10, p, 8, 8, L.BI_BF16, s) == L.BI_ERR_UNSUPPORTED

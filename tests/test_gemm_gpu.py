@@ -328,3 +328,30 @@ def test_pair_tile_stage_shape_keeps_bits(bi, layout):
         ref, nrm = oracle.matmul(a[rows].cpu(), b[:, cols].contiguous().cpu())
     check_close(full[rows][:, cols], ref, nrm, torch.bfloat16, "pair %s 4096 rows" % layout)
     _no_device_error(bi)
+
+
+@pytest.mark.parametrize("layout", ["linear", "matmul"])
+def test_pair_tile_odd_panel_count_keeps_bits(bi, layout):
+    """K = 8256 has an odd number (129) of 64-wide K panels.  With two panels per stage the
+    last stage holds one panel past K; it must not be multiplied, or a row whose
+    accumulator is a signed zero would change bits between the two stage shapes (4096 rows:
+    256 tiles, two panels per stage; 256 rows: 16 tiles, one).  Rows of +0 and of -0
+    are included."""
+    M, N, K = 4096, 4096, 8256
+    a, b = synth.gemm16(M, N, K, "bf16", seed=35, layout=layout, device="cuda")
+    a[5] = 0.0
+    a[6] = -0.0
+    a[7, : K // 2] = -0.0
+    fn = bi.linear if layout == "linear" else bi.matmul
+    full = fn(a, b)
+    assert_same_bits(fn(a[:256], b), full[:256], "%s K=8256 first 256 rows vs all 4096" % layout)
+    for r in (5, 6, 7, 300):
+        assert_same_bits(fn(a[r:r + 1], b), full[r:r + 1], "%s K=8256 row %d alone" % (layout, r))
+    rows = [0, 5, 7, 4095]
+    cols = np.r_[0:32, 4064:4096]
+    if layout == "linear":
+        ref, nrm = oracle.linear(a[rows].cpu(), b[cols].cpu())
+    else:
+        ref, nrm = oracle.matmul(a[rows].cpu(), b[:, cols].contiguous().cpu())
+    check_close(full[rows][:, cols], ref, nrm, torch.bfloat16, "pair %s K=8256" % layout)
+    _no_device_error(bi)
