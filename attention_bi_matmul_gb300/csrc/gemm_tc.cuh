@@ -323,16 +323,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     const uint64_t ad = a_desc0 + s * A_STEP;
                     const uint64_t bd = b_desc0 + s * B_STEP;
 #pragma unroll
-                    for (int p = 0; p < KP; ++p) {
-                        // A panel wholly past K (the last stage when K/64 is odd) is not
-                        // multiplied: every tile issues exactly ceil(K/64) panels.
-                        if (p > 0 && (kb * KP + p) * TC_BK >= K) break;
+                    for (int p = 0; p < KP; ++p)
 #pragma unroll
                         for (int j = 0; j < TC_BK / 16; ++j)
                             mma_f16_ss(d_tmem, ad + p * AP_STEP + j * (32 >> 4),
                                        bd + p * BP_STEP + j * BK_STEP, IDESC,
                                        (kb | p | j) != 0 ? 1u : 0u);
-                    }
                     mma_commit(&empty[s]);
                     if (++s == STAGES) { s = 0; ph ^= 1u; }
                 }
@@ -547,6 +543,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
             const uint64_t A_STEP = A_BYTES >> 4, AP_STEP = A_PANEL >> 4;
             constexpr uint64_t B_STEP = B_BYTES >> 4, BP_STEP = B_PANEL >> 4;
             constexpr uint64_t BK_STEP = B_MN ? (2048 >> 4) : (32 >> 4);
+            const int panels = static_cast<int>((K + TC_BK - 1) / TC_BK);
             uint32_t tc = 0, s = 0, ph = 0;
             bool ok = true;
             for (int64_t t = pair; ok && t < total; t += num_pairs, ++tc) {
@@ -560,17 +557,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
                     tc_fence_after();
                     const uint64_t ad = a_desc0 + s * A_STEP;
                     const uint64_t bd = b_desc0 + s * B_STEP;
+                    // A panel wholly past K is not multiplied, so the MMA sequence of
+                    // a tile is the same with one or two panels per stage (the stage
+                    // shape depends on the number of tiles, hence on M).
+                    const int live = panels - kb * KPP;
 #pragma unroll
                     for (int p = 0; p < KPP; ++p) {
-                        // A panel wholly past K is not multiplied, so the MMA sequence of
-                        // a tile is the same with one or two panels per stage (the stage
-                        // shape depends on the number of tiles, hence on M).
-                        if (p > 0 && (kb * KPP + p) * TC_BK >= K) break;
+                        if (p == 0 || p < live) {
 #pragma unroll
-                        for (int j = 0; j < TC_BK / 16; ++j)
-                            mma_f16_ss_pair(d_tmem, ad + p * AP_STEP + j * (32 >> 4),
-                                            bd + p * BP_STEP + j * BK_STEP, IDESC,
-                                            (kb | p | j) != 0 ? 1u : 0u);
+                            for (int j = 0; j < TC_BK / 16; ++j)
+                                mma_f16_ss_pair(d_tmem, ad + p * AP_STEP + j * (32 >> 4),
+                                                bd + p * BP_STEP + j * BK_STEP, IDESC,
+                                                (kb | p | j) != 0 ? 1u : 0u);
+                        }
                     }
                     mma_commit_pair_mc(&empty[s], 0x3);
                     if (++s == STAGES) { s = 0; ph ^= 1u; }

@@ -96,12 +96,32 @@ def _torch_forward(model, ids, cache, pos0):
         vc[:, :, pos0:pos0 + L] = qkv[:, :, c.H + c.Hkv:].transpose(1, 2)
         k = kc[:, :, :pos0 + L].repeat_interleave(G, 1)
         v = vc[:, :, :pos0 + L].repeat_interleave(G, 1)
-        att = F.scaled_dot_product_attention(q, k, v, is_causal=(L > 1 and pos0 == 0))
+        if L > 1 and pos0 > 0:
+            # a chunk after a cached prefix: query i (position pos0 + i) sees keys j <= pos0 + i
+            vis = (torch.arange(pos0 + L, device=ids.device)[None, :]
+                   <= torch.arange(pos0, pos0 + L, device=ids.device)[:, None])
+            att = F.scaled_dot_product_attention(q, k, v, attn_mask=vis)
+        else:
+            att = F.scaled_dot_product_attention(q, k, v, is_causal=(L > 1 and pos0 == 0))
         h = h + F.linear(att.transpose(1, 2).reshape(B * L, -1), lw["wo"])
         n = F.rms_norm(h, (c.d,), lw["ln2"], c.eps)
         gu = F.linear(n, lw["wgu"])
         h = h + F.linear(F.silu(gu[:, :c.inter]) * gu[:, c.inter:], lw["wdown"])
     return F.linear(F.rms_norm(h, (c.d,), model.lnf, c.eps), model.lm_head).view(B, L, -1)
+
+
+def test_c4_chunked_prefill_matches_one_shot(model, ids):
+    """Decode vs chunked prefill at the decoder level: the 128-token prompt run as one
+    prefill, as two chunks of 64, and as 96 + 32, gives request 0 the same logits bits
+    at every position, and the same KV cache ("mlx-batch-invariant" README, "What
+    batch-invariant means here": query length must not change a token's bits)."""
+    one = model(ids, model.new_cache(8, PROMPT), 0)
+    for split in (64, 96):
+        cache = model.new_cache(8, PROMPT)
+        a = model(ids[:, :split], cache, 0)
+        b = model(ids[:, split:], cache, split)
+        assert_same_bits(a, one[:, :split], "chunked prefill, first %d positions" % split)
+        assert_same_bits(b, one[:, split:], "chunked prefill, positions %d.." % split)
 
 
 def test_c4_torch_control(model, ids):
@@ -120,11 +140,19 @@ def test_c4_torch_control(model, ids):
         counts.append(count_bit_diffs(l1[0, 0], l8[0, 0]))
     print("torch control: logits of request 0 differing (batch 1 vs 8), prefill then decode "
           "steps: %s of %d" % (counts, l1.shape[-1]))
-    # The stock path is allowed to be invariant on these particular shapes (cuBLAS happened to
-    # pick the same kernels for M = 128 vs 1024 and M = 1 vs 8 on GB300); the GEMM and
-    # attention controls of the batch-size and query-length configs show that it is not in
-    # general.  This test records the measurement and checks the control ran to completion.
+    # the query-length axis: one prefill of 128 against chunks of 64 + 64 (batch 8)
+    one = _torch_forward(model, ids, model.new_cache(8, PROMPT), 0)
+    cache = model.new_cache(8, PROMPT)
+    _torch_forward(model, ids[:, :64], cache, 0)
+    two = _torch_forward(model, ids[:, 64:], cache, 64)
+    chunked = count_bit_diffs(two, one[:, 64:])
+    print("torch control: logits differing, one prefill vs chunks of 64 + 64: %d of %d"
+          % (chunked, two.numel()))
     assert len(counts) == STEPS + 1 and torch.isfinite(l1).all() and torch.isfinite(l8).all()
+    # The stock path may happen to be batch-invariant on these shapes (cuBLAS picked the
+    # same kernels for M = 128 vs 1024 and M = 1 vs 8 on GB300); across query lengths it is
+    # not: its attention and GEMM kernels change with the chunk, and the bits move.
+    assert chunked > 0, "stock torch gave identical bits for one prefill and two chunks"
 
 
 def _bf16_sum_bits(a, b):
