@@ -404,6 +404,44 @@ def batch_sweep_per_call(wl, bi, hbm, reps=10, calls=8):
     return out
 
 
+def qlinear_decode(dev, bi, hbm, reps=10, calls=8, N=14336, K=4096, bits=4, gs=64):
+    """The quantized linear at decode shapes (not part of the step): 4-bit group-wise
+    affine weights, N x K, one of 8 weight copies per call (more than L2 holds), as a
+    CUDA graph of `calls` calls replayed `reps` times.  Bytes per call: packed weights,
+    scales and biases, x and y."""
+    import torch
+    from attention_bi_matmul_gb300 import synth
+    copies = [synth.qweights(N, K, bits, gs, "bf16", seed=100 + i, device=dev) for i in range(8)]
+    out = []
+    for M in (1, 16):
+        x = synth.normal((M, K), 99, 1.0, "bf16", dev)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        for i in range(calls):
+            wq, sc, bz = copies[i % 8]
+            bi.qlinear(x, wq, sc, bz, bits, gs, out=y)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(calls):
+                wq, sc, bz = copies[i % 8]
+                bi.qlinear(x, wq, sc, bz, bits, gs, out=y)
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / (reps * calls)
+        nbytes = N * K * bits / 8 + 2 * 2 * N * K / gs + 2 * M * K + 2 * M * N
+        gbs = nbytes / (us * 1e-6) / 1e9
+        out.append({"M": M, "us": round(us, 2), "gbs": round(gbs, 1), "frac_hbm": round(gbs / hbm, 3)})
+    del copies
+    return {"shape": "bi_qlinear %d-bit, group %d, N=%d, K=%d (8 rotating weight copies)" % (bits, gs, N, K),
+            "per_M": out}
+
+
 def decode_gemm_summary(per_call):
     """The decode-shaped GEMM target: M in {1..64}, N = 14336, K = 4096 against HBM."""
     rows = [r for r in per_call if r["N"] == 14336 and r["M"] <= 64]
@@ -605,6 +643,7 @@ def run_ours(args):
     if st != 0:
         raise RuntimeError("device error word %#x after the timed region" % code)
     per_call = None if args.no_per_call else batch_sweep_per_call(wl, bi, hbm)
+    extras = None if args.no_per_call else {"qlinear_decode": qlinear_decode(dev, bi, hbm)}
     step_ms = [ev[s][0].elapsed_time(ev[s][len(parts)]) for s in range(K)]
     coi = cost_of_invariance(wl, dev) if rank == 0 and not args.no_torch_compare else None
 
@@ -692,6 +731,7 @@ def run_ours(args):
                                   "on another while later parts' inputs arrive"},
                "gpu_launches": launches, "clocks": clocks, "cost_of_invariance": coi,
                "decode_gemm": decode_gemm_summary(per_call) if per_call else None,
+               "extras": extras,
                "batch_sweep_per_call": ([[r["N"], r["M"], r["us"], r["frac_hbm"]] for r in per_call]
                                         if per_call else None),
                "batch_sweep_per_call_columns": ["N", "M", "us", "frac_hbm"]}
@@ -793,7 +833,8 @@ def main():
     ap.add_argument("--no-torch-compare", action="store_true",
                     help="skip the comparison with torch / cuBLAS on the same inputs")
     ap.add_argument("--no-per-call", action="store_true",
-                    help="skip the device time of every batch-sweep shape (reported by default)")
+                    help="skip the per-call records: every batch-sweep shape and the quantized "
+                         "linear at decode shapes (reported by default)")
     ap.add_argument("--eager", action="store_true",
                     help="time eager Python calls instead of CUDA-graph replays of each part")
     args = ap.parse_args()
