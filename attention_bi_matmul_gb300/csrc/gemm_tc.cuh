@@ -107,7 +107,11 @@ __device__ __forceinline__ void gemm_epilogue32(const uint32_t (&r)[32], int64_t
 constexpr int TC_BM = 128;
 constexpr int TC_BK = 64;
 constexpr int TC_THREADS = 192;
-constexpr int TC_GROUP_M = 16;
+constexpr int TC_GROUP_M = 16;   // one-CTA tiles: groups of 16 row blocks of 128
+// CTA-pair tiles: groups of 8 row blocks of 256.  Measured at 8192^3 (DRAM bytes
+// per launch, time): 4 -> 1.53 GB, 0.624 ms; 8 -> 1.17 GB, 0.607 ms; 16 -> 1.39 GB,
+// 0.609 ms; 32 -> 2.18 GB, 0.638 ms (algorithmic 0.40 GB).
+constexpr int TC2_GROUP_M = 8;
 
 __host__ __device__ constexpr uint32_t tc_tmem_cols(int bn) {
     // two accumulator buffers of bn fp32 columns, rounded up to a power of two >= 32
@@ -137,17 +141,18 @@ __host__ __device__ constexpr size_t tc_smem_bytes() {
            (2 * TC_MAX_STAGES + 5) * 8 + 16 /* barriers, TMEM slot, abort flag */;
 }
 
-// Tile t -> (batch entry, m block, n block); within an entry, tiles are grouped so
-// that concurrently running tiles share A and B in L2.
+// Tile t -> (batch entry, m block, n block); within an entry, tiles are grouped GM
+// row blocks at a time so that concurrently running tiles share A and B in L2.
+template <int GM = TC_GROUP_M>
 __device__ __forceinline__ void tc_tile_coords(int64_t t, int64_t num_m, int64_t num_n,
                                                int64_t &e, int64_t &mb, int64_t &nb) {
     const int64_t per_entry = num_m * num_n;
     e = t / per_entry;
     t -= e * per_entry;
-    const int64_t in_group = (int64_t)TC_GROUP_M * num_n;
+    const int64_t in_group = (int64_t)GM * num_n;
     const int64_t g = t / in_group;
-    const int64_t first_m = g * TC_GROUP_M;
-    const int64_t gm = (num_m - first_m) < TC_GROUP_M ? (num_m - first_m) : TC_GROUP_M;
+    const int64_t first_m = g * GM;
+    const int64_t gm = (num_m - first_m) < GM ? (num_m - first_m) : GM;
     const int64_t r = t - g * in_group;
     mb = first_m + r % gm;
     nb = r / gm;
@@ -494,7 +499,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
             bool ok = true;
             for (int64_t t = pair; ok && t < total; t += num_pairs) {
                 int64_t e, mb, nb;
-                tc_tile_coords(t, num_m, num_n, e, mb, nb);
+                tc_tile_coords<TC2_GROUP_M>(t, num_m, num_n, e, mb, nb);
                 const int32_t ea = args.sa ? static_cast<int32_t>(e) : 0;
                 const int32_t eb = args.sb ? static_cast<int32_t>(e) : 0;
                 const int32_t row0 = static_cast<int32_t>(mb * TC2_BM + rank * TC_BM);
@@ -589,7 +594,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
         uint32_t tc = 0;
         for (int64_t t = pair; t < total; t += num_pairs, ++tc) {
             int64_t e, mb, nb;
-            tc_tile_coords(t, num_m, num_n, e, mb, nb);
+            tc_tile_coords<TC2_GROUP_M>(t, num_m, num_n, e, mb, nb);
             const uint32_t acc = tc & 1u;
             const uint32_t aph = (tc >> 1) & 1u;
             if (!warp_wait(&tfull[acc], aph, abort_flag)) break;
