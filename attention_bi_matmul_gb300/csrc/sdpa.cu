@@ -49,8 +49,8 @@
 // Roles (320 threads):
 //   warp 0 lane 0   TMA producer (Q once; K and V chunks through 2-deep rings)
 //   warp 1          TMEM allocation (S0, S1 of C columns, O of DP, P0, P1 of
-//                   C/2); lane 0 issues the MMAs, waiting twice per chunk (K_j
-//                   with V_{j-1}, then P_{j-1})
+//                   C/2); lane 0 issues the MMAs, waiting for K_j before S(j)
+//                   and for P_{j-1} and V_{j-1} before P V(j-1)
 //   warps 2..9      row warps: warp w serves TMEM lane quarter w % 4 and half
 //                   (w-2)/4 of the keys (C/2) and of the output columns (DP/2);
 //                   the two warps of a row exchange the chunk maximum and the
@@ -92,8 +92,8 @@ struct S2Smem {
     static constexpr uint32_t MX = V + S2_VST * KV;              // float[2][128] half maxima
     static constexpr uint32_t LS = MX + 2 * 128 * 4;             // float[2][128] half sums
     static constexpr uint32_t BARS = LS + 2 * 128 * 4;
-    // bar_q kvfull[2] sfull[2] pfull[2] pvdone[2] mma_done
-    static constexpr uint32_t NBARS = 1 + 2 + 2 + 2 + 2 + 1;
+    // bar_q kfull[2] vfull[2] sfull[2] pfull[2] pvdone[2] mma_done
+    static constexpr uint32_t NBARS = 1 + 2 + 2 + 2 + 2 + 2 + 1;
     static constexpr uint32_t MISC = BARS + NBARS * 8;           // tmem slot, abort flag
     static constexpr uint32_t END = MISC + 16;
     static constexpr size_t BYTES = 1024 + END;
@@ -133,10 +133,11 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
     float *ls_s = reinterpret_cast<float *>(smem + S2Smem::LS);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S2Smem::BARS);
     uint64_t *bar_q = bars;
-    uint64_t *kvfull = bar_q + 1;        // [2] step j: K_j and V_{j-1} have landed
+    uint64_t *kfull = bar_q + 1;         // [j & 1]: K_j has landed in K slot j % 2
+    uint64_t *vfull = kfull + 2;         // [i & 1]: V_i has landed in V slot i % 2
     // S(j) done: S buffer j & 1 written, and K slot j % 2 read (the producer's
     // release too)
-    uint64_t *sfull = kvfull + 2;        // [2]
+    uint64_t *sfull = vfull + 2;         // [2]
     // [j & 1]: P_j in tensor memory and O rescaled for chunk j.  Two barriers, not one:
     // a row warp with no valid rows may arrive for chunk j + 1 (S(j + 1) is issued
     // before the MMA thread waits for P_j) before the others arrive for chunk j, and
@@ -175,7 +176,10 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
         prefetch_tmap(&tmK);
         prefetch_tmap(&tmV);
         mbar_init(bar_q, 1);
-        for (int s = 0; s < 2; ++s) mbar_init(&kvfull[s], 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&kfull[s], 1);
+            mbar_init(&vfull[s], 1);
+        }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sfull[i], 1);
         }
@@ -191,11 +195,11 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
 #pragma unroll
         for (uint32_t pn = 0; pn < NP; ++pn)
             tma_load_4d(sQ + pn * S2_QPANEL, &tmQ, bar_q, 64 * pn, kvh * G, qi0, b);
-        // step 0 of the loop below: K_0 alone (nchunks >= 1), into K slot 0
-        mbar_arrive_expect_tx(&kvfull[0], S2_KV);
+        // K_0 (nchunks >= 1), into K slot 0
+        mbar_arrive_expect_tx(&kfull[0], S2_KV);
 #pragma unroll
         for (uint32_t pn = 0; pn < NP; ++pn)
-            tma_load_4d(sK + pn * S2_KPANEL, &tmK, &kvfull[0], 64 * pn, 0, kvh, b);
+            tma_load_4d(sK + pn * S2_KPANEL, &tmK, &kfull[0], 64 * pn, 0, kvh, b);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, S2_TMEM_COLS);
@@ -209,48 +213,47 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
-            // Q and step 0 were issued during the block's setup.  Step j loads K_j and
-            // V_{j-1} onto one barrier, so that the MMA thread waits once per chunk for
-            // both (each wait costs the tensor pipe time).
-            // Every step, the last one (V only) included, first waits for S(j-2)
-            // (K slot j % 2 read): the MMA thread issues S(j-2) only after its wait
-            // on step j-2, which used this same barrier, so the barrier is never
-            // armed again before that phase has been consumed.  The V slot waits for
-            // P_{j-3} V_{j-3}.  Both are the MMA's own completion barriers, so it
-            // commits twice per chunk, not four times.
-            int armed = 1;
+            // Q and K_0 were issued during the block's setup.  Step j loads K_j once S(j-2)
+            // is done (K slot j % 2 read), then V_{j-1} once P_{j-3} V_{j-3} is done (V slot
+            // (j-1) % 2 read); each onto its own barrier, so that K_j, which S(j) needs
+            // first, does not wait for a V slot.  The slot releases are the MMA's own
+            // completion barriers.  A fill barrier is armed again only after the MMA that
+            // read its previous contents is done, and the MMA thread waited for that
+            // phase before issuing it, so no phase is armed before it has been consumed.
+            int k_armed = 1, v_armed = 0;    // K_0..K_{k_armed-1}, V_0..V_{v_armed-1} issued
             bool ok = true;
             for (int j = 1; j <= nchunks; ++j) {
-                const bool has_k = j < nchunks, has_v = j >= 1;
-                if (!mbar_wait(&sfull[j & 1], ((j >> 1) & 1u) ^ 1u, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                if (has_v && !mbar_wait(&pvdone[(j - 1) & 1], (((j - 1) >> 1) & 1u) ^ 1u,
-                                        abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                mbar_arrive_expect_tx(&kvfull[j & 1], (has_k ? S2_KV : 0u) + (has_v ? S2_KV : 0u));
-                if (has_k) {
+                if (j < nchunks) {
+                    if (!mbar_wait(&sfull[j & 1], ((j >> 1) & 1u) ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&kfull[j & 1], S2_KV);
 #pragma unroll
                     for (uint32_t pn = 0; pn < NP; ++pn)
-                        tma_load_4d(sK + (j % S2_KST) * S2_KV + pn * S2_KPANEL, &tmK, &kvfull[j & 1],
+                        tma_load_4d(sK + (j % S2_KST) * S2_KV + pn * S2_KPANEL, &tmK, &kfull[j & 1],
                                     64 * pn, j * S2_C, kvh, b);
+                    k_armed = j + 1;
                 }
-                if (has_v) {
+                const int i = j - 1;
+                if (!mbar_wait(&pvdone[i & 1], ((i >> 1) & 1u) ^ 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&vfull[i & 1], S2_KV);
 #pragma unroll
-                    for (uint32_t pn = 0; pn < NP; ++pn)
-                        tma_load_4d(sV + ((j - 1) % S2_VST) * S2_KV + pn * S2_KPANEL, &tmV,
-                                    &kvfull[j & 1], 64 * pn, (j - 1) * S2_C, kvh, b);
-                }
-                armed = j + 1;
+                for (uint32_t pn = 0; pn < NP; ++pn)
+                    tma_load_4d(sV + (i % S2_VST) * S2_KV + pn * S2_KPANEL, &tmV, &vfull[i & 1],
+                                64 * pn, i * S2_C, kvh, b);
+                v_armed = j;
             }
             if (!ok) {
                 // Let every copy already issued land before the block can exit.
                 mbar_wait_limited(bar_q, 0, WAIT_LIMIT_NS);
-                for (int j = armed - 2 < 0 ? 0 : armed - 2; j < armed; ++j)
-                    mbar_wait_limited(&kvfull[j & 1], (j >> 1) & 1u, WAIT_LIMIT_NS);
+                for (int k = k_armed - 2 < 0 ? 0 : k_armed - 2; k < k_armed; ++k)
+                    mbar_wait_limited(&kfull[k & 1], (k >> 1) & 1u, WAIT_LIMIT_NS);
+                for (int k = v_armed - 2 < 0 ? 0 : v_armed - 2; k < v_armed; ++k)
+                    mbar_wait_limited(&vfull[k & 1], (k >> 1) & 1u, WAIT_LIMIT_NS);
             }
         }
     } else if (warp == 1) {
@@ -290,10 +293,9 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
                                (!first || kk > 0) ? 1u : 0u);
             };
             for (int j = 0; ok && j <= nchunks; ++j) {
-                // step j: K_j (if j < nchunks) and V_{j-1} (if j >= 1) have landed
-                if (!mbar_wait(&kvfull[j & 1], (j >> 1) & 1u, abort_flag)) { ok = false; break; }
-                tc_fence_after();
                 if (j < nchunks) {
+                    if (!mbar_wait(&kfull[j & 1], (j >> 1) & 1u, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
                     // S(j) = Q K_j^T into S buffer j & 1 (DP / 16 steps over the head dim).
                     // That buffer held S(j-2), which the row warps read before writing
                     // P(j-2), whose barrier this thread waited for at step j-1.
@@ -305,7 +307,8 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
                 if (j >= 1) {
                     // O (+)= P_i V_i, i = j - 1 (the rows rescaled O before signalling)
                     const int i = j - 1;
-                    if (!mbar_wait(&pfull[i & 1], (i >> 1) & 1u, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(&pfull[i & 1], (i >> 1) & 1u, abort_flag) ||
+                        !mbar_wait(&vfull[i & 1], (i >> 1) & 1u, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t p_tmem = tmem_base + S2_P_COL + (i & 1) * (C / 2);
                     if (i % S2_VST == 0) issue_pv(vd[0], p_tmem, i == 0);

@@ -15,7 +15,7 @@ commits behind them).  For every run the model checks:
 * nothing deadlocks.
 
 Planted mistakes (one P barrier instead of two, no wait before the O rescale, no
-wait before a V slot is refilled) must be caught: that is what makes the clean runs
+wait before a K or a V slot is refilled) must be caught: that is what makes the clean runs
 mean something.  The model also shows that the row warps need no wait before
 overwriting P_{j-2}: S(j)'s commit, which they wait for, arrives only after every
 MMA issued before it -- P_{j-2} V_{j-2} included -- has completed.
@@ -53,13 +53,16 @@ class Model:
     """One CTA of the kernel with `n` key chunks; `valid[w]` says whether row warp w holds
     any valid query row (decode: only the rows of one lane quarter)."""
 
-    def __init__(self, n, valid, rng, single_pfull=False, no_rescale_wait=False, no_v_slot_wait=False):
+    def __init__(self, n, valid, rng, single_pfull=False, no_rescale_wait=False, no_v_slot_wait=False,
+                 no_k_slot_wait=False):
         self.n, self.valid, self.rng = n, valid, rng
         self.single_pfull = single_pfull
         self.no_rescale_wait, self.no_v_slot_wait = no_rescale_wait, no_v_slot_wait
+        self.no_k_slot_wait = no_k_slot_wait
         B = Barrier
         self.bar_q = B("q", 1)
-        self.kvfull = [B("kvfull0", 1), B("kvfull1", 1)]
+        self.kfull = [B("kfull0", 1), B("kfull1", 1)]
+        self.vfull = [B("vfull0", 1), B("vfull1", 1)]
         self.sfull = [B("sfull0", 1), B("sfull1", 1)]
         self.pfull = [B("pfull0", 8)] if single_pfull else [B("pfull0", 8), B("pfull1", 8)]
         self.pvdone = [B("pvdone0", 1), B("pvdone1", 1)]
@@ -105,32 +108,32 @@ class Model:
     def producer(self):
         n = self.n
         self.pending.append((self.bar_q, lambda: self.landed.add("Q")))
+        self.pending.append((self.kfull[0], lambda: self.landed.add(("K", 0))))
         yield "step"
-        for j in range(n + 1):
-            # K slot j % 2 free: S(j-2) done (a fresh barrier with parity 1 passes at once)
-            yield from self.wait(self.sfull[j & 1], ((j >> 1) & 1) ^ 1, (j >> 1) - 1, "producer")
-            if j >= 1 and not self.no_v_slot_wait:
-                yield from self.wait(self.pvdone[(j - 1) & 1], (((j - 1) >> 1) & 1) ^ 1, ((j - 1) >> 1) - 1,
-                                     "producer")
-            if j < n and j >= 2:
-                self.need(j - 2 in self.s_done, "K slot %d refilled before S(%d) read it" % (j % 2, j - 2))
-            if j >= 1 and j - 3 >= 0:
-                self.need(j - 3 in self.pv_done, "V slot %d refilled before P V(%d) read it" % ((j - 1) % 2, j - 3))
-
-            def land(j=j):
-                if j < n:
-                    self.landed.add(("K", j))
-                if j >= 1:
-                    self.landed.add(("V", j - 1))
-            self.pending.append((self.kvfull[j & 1], land))
+        for j in range(1, n + 1):
+            if j < n:
+                # K slot j % 2 free: S(j-2) done (a fresh barrier with parity 1 passes at once)
+                if not self.no_k_slot_wait:
+                    yield from self.wait(self.sfull[j & 1], ((j >> 1) & 1) ^ 1, (j >> 1) - 1, "producer")
+                if j >= 2:
+                    self.need(j - 2 in self.s_done, "K slot %d refilled before S(%d) read it" % (j % 2, j - 2))
+                self.pending.append((self.kfull[j & 1], lambda j=j: self.landed.add(("K", j))))
+                yield "step"
+            # V slot i % 2 free: P V(i-2) done
+            i = j - 1
+            if not self.no_v_slot_wait:
+                yield from self.wait(self.pvdone[i & 1], ((i >> 1) & 1) ^ 1, (i >> 1) - 1, "producer")
+            if i >= 2:
+                self.need(i - 2 in self.pv_done, "V slot %d refilled before P V(%d) read it" % (i % 2, i - 2))
+            self.pending.append((self.vfull[i & 1], lambda i=i: self.landed.add(("V", i))))
             yield "step"
 
     def mma(self):
         n = self.n
         yield from self.wait(self.bar_q, 0, 0, "mma")
         for j in range(n + 1):
-            yield from self.wait(self.kvfull[j & 1], (j >> 1) & 1, j >> 1, "mma")
             if j < n:
+                yield from self.wait(self.kfull[j & 1], (j >> 1) & 1, j >> 1, "mma")
                 self.need("Q" in self.landed and ("K", j) in self.landed, "S(%d) issued before Q/K landed" % j)
                 if j >= 2:
                     self.need(len(self.s_read.get(j - 2, ())) == 8, "S(%d) overwrites S(%d) before all rows read it" % (j, j - 2))
@@ -143,6 +146,7 @@ class Model:
                     yield from self.wait(self.pfull[0], i & 1, i, "mma")
                 else:
                     yield from self.wait(self.pfull[i & 1], (i >> 1) & 1, i >> 1, "mma")
+                yield from self.wait(self.vfull[i & 1], (i >> 1) & 1, i >> 1, "mma")
                 writers = self.p_written.get(i, set())
                 need = {w for w in range(8) if self.valid[w]}
                 self.need(need <= writers, "P V(%d) issued before P_%d was written by warps %s" % (i, i, sorted(need - writers)))
@@ -255,7 +259,7 @@ def test_protocol_holds(pattern):
     run_many({pattern: PATTERNS[pattern]}, range(1, 11), range(40))
 
 
-@pytest.mark.parametrize("mutation", ["single_pfull", "no_rescale_wait", "no_v_slot_wait"])
+@pytest.mark.parametrize("mutation", ["single_pfull", "no_rescale_wait", "no_v_slot_wait", "no_k_slot_wait"])
 def test_planted_protocol_mistakes_are_caught(mutation):
     with pytest.raises(Hazard):
         run_many(PATTERNS, range(2, 11), range(40), **{mutation: True})
