@@ -101,6 +101,28 @@ def test_sliding_window_parity(bi):
     check_close(o, ref, nrm, torch.bfloat16, "sdpa sliding window + sinks")
 
 
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("with_sinks", [False, True])
+def test_late_rescales_parity_and_repeat(bi, causal, with_sinks):
+    """Keys whose scores grow along the sequence, so that a row's shift moves up again
+    and again in late chunks and O is rescaled between P V steps near the end of the
+    call -- the case where a wait for the last P V could pass before an earlier one
+    finished.  Parity with the oracle, and two calls bit for bit equal."""
+    B, H, Hkv, Lq, Lkv = 2, 8, 2, 300, 1000
+    q, k, v = synth.sdpa_qkv(B, H, Hkv, Lq, Lkv, 128, "bf16", seed=77)
+    grow = 1.0 + 8.0 * torch.arange(Lkv, dtype=torch.float32).view(1, 1, Lkv, 1) / Lkv
+    k = (k.float() * grow).to(torch.bfloat16)
+    sk = _sinks(H, 5) if with_sinks else None
+    qc, kc, vc = q.cuda(), k.cuda(), v.cuda()
+    skc = sk.cuda() if with_sinks else None
+    o1 = bi.sdpa(qc, kc, vc, causal=causal, sinks=skc)
+    o2 = bi.sdpa(qc, kc, vc, causal=causal, sinks=skc)
+    assert_same_bits(o1, o2, "late rescales, two calls")
+    ref, nrm = oracle.sdpa_ex(q, k, v, causal=causal, sinks=sk)
+    check_close(o1, ref, nrm, torch.bfloat16, "late rescales causal=%s sinks=%s" % (causal, with_sinks))
+    _no_device_error(bi)
+
+
 # ------------------------------------------------------------------ degenerate rows
 
 def test_fully_masked_rows(bi):
