@@ -102,8 +102,8 @@ struct S2Smem {
     static constexpr uint32_t MX = V + S2_VST * KV;              // float[2][128] half maxima
     static constexpr uint32_t LS = MX + 2 * 128 * 4;             // float[2][128] half sums
     static constexpr uint32_t BARS = LS + 2 * 128 * 4;
-    // bar_q kfull[2] vfull[2] sfull[3] pfull[3] pvdone[4] mma_done
-    static constexpr uint32_t NBARS = 1 + 2 + 2 + 3 + 3 + 4 + 1;
+    // bar_q kfull[2] vfull[2] sfull[3] pfull[3] phi[3] pvdone[4] mma_done
+    static constexpr uint32_t NBARS = 1 + 2 + 2 + 3 + 3 + 3 + 4 + 1;
     static constexpr uint32_t MISC = BARS + NBARS * 8;           // tmem slot, abort flag
     static constexpr uint32_t END = MISC + 16;
     static constexpr size_t BYTES = 1024 + END;
@@ -155,7 +155,11 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
     // Four barriers: S(i+3), which the S thread issues only after P V(i) is done, may
     // let P V(i+1) .. P V(i+2) run while a waiter is still at P V(i)'s phase; with four
     // entries no barrier can move two phases ahead of a wait.
-    uint64_t *pvdone = pfull + 3;
+    // [j % 3]: P_j of the chunk's upper half of keys (C/2..C-1) in tensor memory; pfull
+    // covers the lower half and the rescale, so that the P V MMAs of the lower half go
+    // out while the rows still work on the upper one.  Same argument as for pfull.
+    uint64_t *phi = pfull + 3;
+    uint64_t *pvdone = phi + 3;
     uint64_t *mma_done = pvdone + 4;    // every P V done (the last, and so every S before it)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S2Smem::MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S2Smem::MISC + 4);
@@ -193,7 +197,8 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
         for (int i = 0; i < 4; ++i) mbar_init(&pvdone[i], 1);
         for (int i = 0; i < 3; ++i) {
             mbar_init(&sfull[i], 1);
-            mbar_init(&pfull[i], 8);
+            mbar_init(&pfull[i], 4);
+            mbar_init(&phi[i], 4);
         }
         mbar_init(mma_done, 1);
         *abort_flag = 0;
@@ -327,11 +332,13 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
 #pragma unroll
                 for (int sl = 0; sl < 2; ++sl)
                     vd[sl][kk] = smem_desc(smem_u32(sV + sl * S2_KV) + kk * 2048, S2_KPANEL, 1024);
-            auto issue_pv = [&](const uint64_t (&vds)[NV], uint32_t p_tmem, bool first) {
+            // K = 16 steps kk0..kk1-1 of P_i V_i, in ascending order
+            auto issue_pv = [&](const uint64_t (&vds)[NV], uint32_t p_tmem, bool first, int kk0, int kk1) {
 #pragma unroll
                 for (int kk = 0; kk < NV; ++kk)
-                    mma_f16_ts(tmem_base + S2_O_COL, p_tmem + (kk / KPH) * HK + (kk % KPH) * 8, vds[kk],
-                               IDESC_PV, (!first || kk > 0) ? 1u : 0u);
+                    if (kk >= kk0 && kk < kk1)
+                        mma_f16_ts(tmem_base + S2_O_COL, p_tmem + (kk / KPH) * HK + (kk % KPH) * 8, vds[kk],
+                                   IDESC_PV, (!first || kk > 0) ? 1u : 0u);
             };
             bool ok = true;
             for (int i = 0; ok && i < nchunks; ++i) {
@@ -342,8 +349,15 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t p_tmem = tmem_base + static_cast<uint32_t>(i % 3) * S2_C;
-                if (i % S2_VST == 0) issue_pv(vd[0], p_tmem, i == 0);
-                else issue_pv(vd[1], p_tmem, i == 0);
+                if (i % S2_VST == 0) issue_pv(vd[0], p_tmem, i == 0, 0, NV / 2);
+                else issue_pv(vd[1], p_tmem, i == 0, 0, NV / 2);
+                if (!mbar_wait(&phi[i % 3], static_cast<uint32_t>(i / 3) & 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (i % S2_VST == 0) issue_pv(vd[0], p_tmem, i == 0, NV / 2, NV);
+                else issue_pv(vd[1], p_tmem, i == 0, NV / 2, NV);
                 mma_commit(&pvdone[i % 4]);
             }
             // P V(n-1) follows S(n-1) (its P needs S(n-1)), so this covers every MMA.
@@ -353,7 +367,7 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
     } else if (warp >= SDPA_ROW_WARP0 && warp < SDPA_ROW_WARP0 + 8) {
         sdpa_rows<T, ARR, DP, C>(args, warp, lane, tmem_base, p_lo, kvh, b, nchunks, sfull, pvdone,
                                  mma_done, mx_s, ls_s, abort_flag,
-                                 [&](uint32_t sb) { mbar_arrive(&pfull[sb]); });
+                                 [&](uint32_t sb, int part) { mbar_arrive(part == 0 ? &pfull[sb] : &phi[sb]); });
     }
 
     __syncthreads();
