@@ -22,9 +22,13 @@
 //     if x > m + 8, and otherwise stays (m' = m): the shift may lag the
 //     running maximum by up to 8, so p <= 2^8, and most chunks leave it and
 //     the accumulator alone; alpha = 2^(m - m') (exactly 1 when m' = m);
-//     p_j = 2^(fma(s_j, c, -m')); l = l * alpha + (half sum + half sum), each
-//     half summed as four interleaved partial sums (key mod 4) added as
-//     (0+1)+(2+3); P rounded to the input dtype;
+//     p_j = 2^(fma(s_j, c, -m')); P rounded to the input dtype.  The row sum is
+//     kept as two partial sums, one over the even chunks and one over the odd
+//     ones, added once at the end (even first): each takes
+//     l_e = l_e * alpha + chunk sum at its own chunks and l_e = l_e * alpha at
+//     the others; a chunk sum is (sum of keys 0..63 + sum of keys 64..127) for
+//     C = 128 and the sum of its 64 keys for C = 64, each such sum taken as four
+//     interleaved partial sums (key mod 4) added as (0+1)+(2+3);
 //   * P is written into tensor memory, over the chunk's own S columns, and read from
 //     there by the P V MMA (its A operand); the output is one fp32 accumulator in
 //     tensor memory that the
@@ -40,7 +44,7 @@
 //   * o = acc * (1 / l) (the reciprocal correctly rounded, then one fp32 multiply),
 //     rounded once to the output dtype;
 //   * an attention sink (one extra logit per head, no value) enters as the
-//     initial state m = sink * log2 e, l = 1.
+//     initial state m = sink * log2 e and 1 in the even chunks' sum.
 // Head dims that are not a multiple of 64 are loaded with the copy engine's zero
 // fill past D (they add exact zeros to Q K^T) and the columns past D are never
 // stored.  Every quantity of a row depends only on that row's query, the keys and
@@ -53,16 +57,21 @@
 //                   lane 0 issues S(t) into buffer t % 3 once K_t has landed and
 //                   P V(t-3) is done, so S runs up to three chunks ahead of P V
 //   warps 2..9      row warps (sdpa_rows.cuh): warp w serves TMEM lane quarter w % 4
-//                   and half (w-2)/4 of the keys (C/2) and of the output columns
-//                   (DP/2); the two warps of a row exchange the chunk maximum and
-//                   the half sums through shared memory (named barrier per quarter)
+//                   and the chunks j with j % 2 == (w-2)/4, all keys of each; the
+//                   two warps of a quarter pass the shift on through a named
+//                   barrier per direction, and each writes half of the output
+//                   columns (DP/2) at the end
 //   warp 10 lane 0  V producer (the V ring 2 deep), apart from K so that a V slot
 //                   released late never holds back a K chunk
-//   warp 11 lane 0  issues P V(i) once the rows have written P_i and V_i has landed
+//   warp 11 lane 0  issues P V(i) once V_i has landed, the MMAs of the lower half of
+//                   the keys once the rows have written that half of P_i, the rest
+//                   once they have written the upper half
 // Measured on B4 H32/8 L4096 D128 causal: one thread issuing both kinds of MMA in
 // alternation kept the rows waiting about 0.3 us per chunk for S (the chain
 // P_{j-1} -> P V(j-1) -> S(j+1) lay on every chunk's path); with separate S and P V
-// threads and three S buffers the call went from 0.528 to 0.477 ms.
+// threads and three S buffers the call went from 0.528 to 0.477 ms; with the chunks
+// taken in turn by the two warps of a quarter (no longer in step with each other) and
+// P published in halves, to 0.466 ms (D 64: 0.454 to 0.398 ms).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 

@@ -45,8 +45,9 @@ __device__ __forceinline__ void shift_receive(int from_grp, uint32_t quarter) {
 }
 
 // One row warp's whole share of a query tile: for each of its chunks j, S from
-// sfull[j % 3], P_j written and O rescaled (after P V(j-1), pvdone[(j-1) % 4]) before
-// arrive_p(j % 3); the output read once every MMA is done (mma_done, one phase).
+// sfull[j % 3], O rescaled (after P V(j-1), pvdone[(j-1) % 4]), then P_j written and
+// published in two halves, arrive_p(j % 3, 0) for keys 0..C/2-1 and arrive_p(j % 3, 1)
+// for the rest; the output read once every MMA is done (mma_done, one phase).
 // p_lo: absolute position of the tile's first query row.
 //
 // S(j) is issued only after P V(j-3) is done, so at chunk j pvdone[(j-1) % 4]'s phase

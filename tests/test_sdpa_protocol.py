@@ -3,28 +3,37 @@ random interleavings.
 
 The kernel's roles -- a K copy producer, a V copy producer, a thread that issues the
 S = Q K^T MMAs, a thread that issues the P V MMAs, eight row warps (two per TMEM lane
-quarter) -- are modelled as coroutines over mbarriers with the hardware's parity
-semantics: a wait for parity P returns as soon as the phase in progress has the other
-parity.  Copies land in any order.  Each issuing thread's MMAs complete in its issue
-order and its commits arrive behind them, but the two threads' MMAs may complete in
-any interleaving (the model assumes nothing about order across threads).  For every
-run the model checks:
+quarter, which take the chunks in turn) -- are modelled as coroutines over mbarriers
+with the hardware's parity semantics: a wait for parity P returns as soon as the phase
+in progress has the other parity.  Copies land in any order.  Each issuing thread's
+MMAs complete in its issue order and its commits arrive behind them, but the two
+threads' MMAs may complete in any interleaving (the model assumes nothing about order
+across threads).  The two warps of a lane quarter hand the running shift over through
+a named barrier per direction (the chooser arrives, the other waits) and meet at a
+third at the end; a named barrier completes when both warps have arrived, so a warp
+that arrived twice before the other waits would break it.  For every run the model
+checks:
 
 * no wait can be satisfied by the wrong phase (its barrier one phase behind) or be
   left waiting for a phase two ahead of the one meant;
 * every buffer is written only after its last reader is done and read only after its
   writer is done: the K and V ring slots, the three S buffers (S(j), then P_j written
-  over it by the rows), and O (rescaled by the rows between two P V MMAs, read out at
-  the end);
-* each phase of a P barrier is made of the arrivals of a single chunk;
+  over it by the rows in two halves, each read by its own P V MMAs), the shift slots,
+  and O (rescaled by the rows before a chunk's P V, read out at the end);
+* the shifts are chosen in chunk order: a warp chooses chunk j's after it has taken
+  chunk j-1's from the other warp;
+* each phase of a P barrier is made of the arrivals of a single chunk; every named
+  barrier ends with no arrival left waiting;
 * nothing deadlocks.
 
 Planted mistakes must be caught, which is what makes the clean runs mean something:
 two P V barriers instead of four (with two, a parity wait for P V(i) can pass while
 P V(i-2) is still running), S(t) not waiting for P V(t-3), two P barriers instead of
-three, and a missing wait before a K slot, a V slot or the O rescale.  With four P V
-barriers the read-out could also wait on the last P V's barrier (the model shows it
-safe: `readout_on_pvdone`); the kernel waits on the all-done barrier.
+three, a missing wait before a K slot, a V slot, the O rescale or the upper half's
+P V MMAs, P barriers counting all eight warps, one shared shift barrier for both
+directions, and the last shift left untaken.  With four P V barriers the read-out
+could also wait on the last P V's barrier (the model shows it safe:
+`readout_on_pvdone`); the kernel waits on the all-done barrier.
 """
 import random
 
@@ -55,35 +64,72 @@ class Barrier:
         return (self.done & 1) != parity
 
 
+class NamedBarrier:
+    """A hardware named barrier over the two warps of a lane quarter: it completes when
+    both have arrived (arrive does not wait, sync does).  An arrival by a warp that
+    already arrived in the phase in progress would complete it without the other."""
+
+    def __init__(self, name):
+        self.name, self.phase, self.arrived = name, 0, []
+
+    def _add(self, w):
+        if w in self.arrived:
+            raise Hazard("%s: warp %d arrives twice in one phase" % (self.name, w))
+        self.arrived.append(w)
+        if len(self.arrived) == 2:
+            self.arrived, self.phase = [], self.phase + 1
+
+    def arrive(self, w):
+        self._add(w)
+
+    def sync(self, w):
+        ph = self.phase
+        self._add(w)
+        while self.phase == ph:
+            yield "blocked"
+
+
 class Model:
     """One CTA with `n` key chunks; `valid[w]` says whether row warp w holds any valid
-    query row (decode: only the rows of one lane quarter)."""
+    query row (decode: only the rows of one lane quarter).  Row warp w serves lane
+    quarter w % 4 and the chunks j with j % 2 == w // 4."""
 
-    def __init__(self, n, valid, rng, n_pvdone=4, n_pfull=3, readout_on_pvdone=False,
+    def __init__(self, n, valid, rng, n_pvdone=4, n_pfull=3, p_count=4, readout_on_pvdone=False,
                  no_s_wait=False, no_k_slot_wait=False, no_v_slot_wait=False,
-                 no_rescale_wait=False):
+                 no_rescale_wait=False, no_phi_wait=False, one_shift_barrier=False,
+                 skip_last_receive=False):
         self.n, self.valid, self.rng = n, valid, rng
         self.n_pvdone, self.n_pfull = n_pvdone, n_pfull
         self.readout_on_pvdone, self.no_s_wait = readout_on_pvdone, no_s_wait
         self.no_k_slot_wait, self.no_v_slot_wait = no_k_slot_wait, no_v_slot_wait
-        self.no_rescale_wait = no_rescale_wait
+        self.no_rescale_wait, self.no_phi_wait = no_rescale_wait, no_phi_wait
+        self.skip_last_receive = skip_last_receive
         B = Barrier
         self.bar_q = B("q", 1)
         self.kfull = [B("kfull%d" % i, 1) for i in range(2)]
         self.vfull = [B("vfull%d" % i, 1) for i in range(2)]
         self.sfull = [B("sfull%d" % i, 1) for i in range(3)]
-        self.pfull = [B("pfull%d" % i, 8) for i in range(n_pfull)]
+        self.pfull = [B("pfull%d" % i, p_count) for i in range(n_pfull)]
+        self.phi = [B("phi%d" % i, p_count) for i in range(n_pfull)]
         self.pvdone = [B("pvdone%d" % i, 1) for i in range(n_pvdone)]
         self.mma_done = B("mma_done", 1)
+        # named barriers per lane quarter: the shift chosen by group g, and the end meeting
+        self.shift_bar = {}
+        for q in range(4):
+            b0 = NamedBarrier("shift q%d g0" % q)
+            b1 = b0 if one_shift_barrier else NamedBarrier("shift q%d g1" % q)
+            self.shift_bar[(q, 0)], self.shift_bar[(q, 1)] = b0, b1
+        self.end_bar = [NamedBarrier("end q%d" % q) for q in range(4)]
         self.pending = []                       # copies in flight: (barrier, action)
         self.pipe = {"S": [], "PV": []}         # per issuing thread, in issue order
         # data state
         self.landed = set()                     # ("K", j), ("V", i), "Q"
         self.s_done, self.pv_done = set(), set()
-        self.s_read = {}                        # j -> row warps that read S(j)
-        self.p_written = {}                     # j -> row warps that wrote P_j
-        self.named = {}
+        self.pv_lo_issued, self.pv_lo_done = set(), set()
+        self.p_written = {}                     # (j, half) -> row warps that wrote it
         self.rescale = {}
+        self.shift_slot = {}                    # (quarter, slot) -> [chunk, taken]
+        self.shift_known = {}                   # warp -> last chunk whose shift it holds
 
     # -- checks ---------------------------------------------------------------------
     def need(self, cond, what):
@@ -100,19 +146,11 @@ class Model:
                 return
             yield "blocked"
 
-    def named_sync(self, quarter):
-        gen_waiting = self.named.setdefault(quarter, [0, 0])
-        gen = gen_waiting[0]
-        gen_waiting[1] += 1
-        if gen_waiting[1] == 2:
-            gen_waiting[0] += 1
-            gen_waiting[1] = 0
-            return
-        while self.named[quarter][0] == gen:
-            yield "blocked"
-
     def pvbar(self, i):
         return self.pvdone[i % self.n_pvdone], (i // self.n_pvdone) & 1, i // self.n_pvdone
+
+    def pbar(self, bars, j):
+        return bars[j % self.n_pfull], (j // self.n_pfull) & 1, j // self.n_pfull
 
     # -- roles ----------------------------------------------------------------------
     def k_producer(self):
@@ -149,51 +187,80 @@ class Model:
             self.pipe["S"].append(("commit", self.sfull[t % 3]))
             yield "step"
 
+    def writers_needed(self, j):
+        return {w for w in range(8) if self.valid[w] and w // 4 == j % 2}
+
     def pv_thread(self):
         for i in range(self.n):
-            yield from self.wait(self.pfull[i % self.n_pfull], (i // self.n_pfull) & 1, i // self.n_pfull, "PV")
+            yield from self.wait(*self.pbar(self.pfull, i), "PV")
             yield from self.wait(self.vfull[i & 1], (i >> 1) & 1, i >> 1, "PV")
-            need = {w for w in range(8) if self.valid[w]}
-            writers = self.p_written.get(i, set())
-            self.need(need <= writers, "P V(%d) issued before P_%d was written by warps %s" % (i, i, sorted(need - writers)))
+            need, writers = self.writers_needed(i), self.p_written.get((i, 0), set())
+            self.need(need <= writers, "P V(%d) lower half issued before warps %s wrote it" % (i, sorted(need - writers)))
             self.need(("V", i) in self.landed, "P V(%d) issued before V_%d landed" % (i, i))
+            self.pv_lo_issued.add(i)
+            self.pipe["PV"].append(("op", "PVlo", i))
+            yield "step"
+            if not self.no_phi_wait:
+                yield from self.wait(*self.pbar(self.phi, i), "PV")
+            writers = self.p_written.get((i, 1), set())
+            self.need(need <= writers, "P V(%d) upper half issued before warps %s wrote it" % (i, sorted(need - writers)))
             self.pipe["PV"].append(("op", "PV", i))
             bar, _, _ = self.pvbar(i)
             self.pipe["PV"].append(("commit", bar))
             yield "step"
         self.pipe["PV"].append(("commit", self.mma_done))
 
+    def receive(self, w, jp):
+        q, g = w % 4, w // 4
+        yield from self.shift_bar[(q, g ^ 1)].sync(w)
+        slot = self.shift_slot.get((q, jp & 1))
+        self.need(slot is not None and slot[0] == jp, "row %d took the shift of chunk %d from a slot holding %s" % (w, jp, slot))
+        slot[1] = True
+        self.shift_known[w] = jp
+
     def row_warp(self, w):
-        n, quarter = self.n, w % 4
-        for j in range(n):
+        n, q, grp = self.n, w % 4, w // 4
+        self.shift_known[w] = -1
+        for j in range(grp, n, 2):
             yield from self.wait(self.sfull[j % 3], (j // 3) & 1, j // 3, "row%d" % w)
             self.need(j in self.s_done, "row %d read S(%d) before it was complete" % (w, j))
-            self.s_read.setdefault(j, set()).add(w)
             yield "step"
-            yield from self.named_sync(quarter)
-            if self.valid[w]:
-                key = (quarter, j)
-                if key not in self.rescale:
-                    self.rescale[key] = j >= 1 and self.rng.random() < 0.3
-                # P_j over S buffer j % 3 (already read by this warp)
-                self.p_written.setdefault(j, set()).add(w)
+            if j >= 1:
+                yield from self.receive(w, j - 1)
+            self.need(self.shift_known[w] == j - 1, "row %d chose chunk %d's shift before taking chunk %d's" % (w, j, j - 1))
+            old = self.shift_slot.get((q, j & 1))
+            self.need(old is None or old[1], "row %d overwrote the shift of chunk %d before it was taken" % (w, old[0] if old else -1))
+            self.shift_slot[(q, j & 1)] = [j, False]
+            self.shift_known[w] = j
+            self.shift_bar[(q, grp)].arrive(w)
+            yield "step"
+            key = (q, j)
+            if key not in self.rescale:
+                self.rescale[key] = j >= 1 and self.rng.random() < 0.3
+            if self.valid[w] and self.rescale[key]:
+                if not self.no_rescale_wait:
+                    bar, par, k = self.pvbar(j - 1)
+                    yield from self.wait(bar, par, k, "row%d" % w)
+                self.need(j - 1 in self.pv_done, "row %d rescaled O before P V(%d) was done" % (w, j - 1))
+                self.need(j not in self.pv_lo_issued, "O rescaled for chunk %d after its P V started" % j)
                 yield "step"
-                if self.rescale[key]:
-                    if not self.no_rescale_wait:
-                        bar, par, k = self.pvbar(j - 1)
-                        yield from self.wait(bar, par, k, "row%d" % w)
-                    self.need(j - 1 in self.pv_done, "row %d rescaled O before P V(%d) was done" % (w, j - 1))
-                    self.need(j not in self.pv_done, "O rescaled for chunk %d after its P V" % j)
+            for half, bars in ((0, self.pfull), (1, self.phi)):
+                if self.valid[w]:
+                    # P_j's half over S buffer j % 3, which this warp has read out
+                    self.p_written.setdefault((j, half), set()).add(w)
                     yield "step"
-            self.pfull[j % self.n_pfull].arrive(j)
-            yield "step"
-            yield from self.named_sync(quarter)
+                bars[j % self.n_pfull].arrive(j)
+                yield "step"
+        if n >= 1 and (n - 1) % 2 != grp and not self.skip_last_receive:
+            yield from self.receive(w, n - 1)
+        yield from self.end_bar[q].sync(w)
         if self.readout_on_pvdone:
             bar, par, k = self.pvbar(n - 1)
             yield from self.wait(bar, par, k, "row%d" % w)
         else:
             yield from self.wait(self.mma_done, 0, 0, "row%d" % w)
         self.need(all(i in self.pv_done for i in range(n)), "row %d read O before every P V was done" % w)
+        self.need(self.shift_known[w] == n - 1, "row %d ended without the last chunk's shift" % w)
 
     # -- asynchronous engines --------------------------------------------------------
     def engine_step(self):
@@ -220,6 +287,8 @@ class Model:
                 if idx >= 3:
                     self.need(idx - 3 in self.pv_done, "S(%d) overwrote P_%d before P V(%d) was done" % (idx, idx - 3, idx - 3))
                 self.s_done.add(idx)
+            elif name == "PVlo":
+                self.pv_lo_done.add(idx)
             else:
                 self.pv_done.add(idx)
         else:
@@ -252,9 +321,11 @@ class Model:
                 raise Hazard("deadlock with agents %s blocked" % live)
         else:
             raise Hazard("did not finish")
-        for b in self.pfull:
+        for b in self.pfull + self.phi:
             for ph, tags in enumerate(b.phase_tags):
                 self.need(len(set(tags)) == 1, "%s phase %d mixes chunks %s" % (b.name, ph, sorted(set(tags))))
+        for nb in list(self.shift_bar.values()) + self.end_bar:
+            self.need(not nb.arrived, "%s ends with warps %s left arrived" % (nb.name, nb.arrived))
 
 
 PATTERNS = {
@@ -284,6 +355,10 @@ MUTATIONS = {
     "no K slot wait": dict(no_k_slot_wait=True),
     "no V slot wait": dict(no_v_slot_wait=True),
     "no rescale wait": dict(no_rescale_wait=True),
+    "no wait for the upper half of P": dict(no_phi_wait=True),
+    "P barriers counting eight warps": dict(p_count=8),
+    "one shift barrier for both directions": dict(one_shift_barrier=True),
+    "last shift left untaken": dict(skip_last_receive=True),
 }
 
 
