@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
         for (uint32_t pn = 0; pn < NP; ++pn)
             tma_load_4d(sK + pn * S2_KPANEL, &tmK, &kfull[0], 64 * pn, 0, kvh, b);
         // Blocks start in about their linear order, one per SM at a time, so the block
-        // that runs on an SM about one round after this one is some %nsmid blocks on.
+        // that runs on an SM about one wave after this one is some %nsmid blocks on.
         // Bringing its Q tile into L2 now (a hint; nothing waits for it) takes its first
         // copy off HBM latency: ~1.3 % on causal prefill.
         {
