@@ -109,8 +109,8 @@ struct S2Smem {
     static constexpr uint32_t K = Q + QB;
     static constexpr uint32_t V = K + S2_KST * KV;
     static constexpr uint32_t MX = V + S2_VST * KV;              // float[2][128] half maxima
-    static constexpr uint32_t LS = MX + 2 * 128 * 4;             // float[2][128] half sums
-    static constexpr uint32_t BARS = LS + 2 * 128 * 4;
+    // (the two row sums of a row meet, at the very end, in K slot 0)
+    static constexpr uint32_t BARS = MX + 2 * 128 * 4;
     // bar_q kfull[2] vfull[2] sfull[3] pfull[3] phi[3] pvdone[4] mma_done
     static constexpr uint32_t NBARS = 1 + 2 + 2 + 3 + 3 + 3 + 4 + 1;
     static constexpr uint32_t MISC = BARS + NBARS * 8;           // tmem slot, abort flag
@@ -145,7 +145,11 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
     uint8_t *sK = smem + S2Smem::K;
     uint8_t *sV = smem + S2Smem::V;
     float *mx_s = reinterpret_cast<float *>(smem + S2Smem::MX);
-    float *ls_s = reinterpret_cast<float *>(smem + S2Smem::LS);
+    // The two warps of a lane quarter add their row sums once, after their last chunk:
+    // by then S of the last chunk is done, so no copy or MMA touches K slot 0 any more,
+    // and the 1 KB exchange lives there.  One KB less keeps the block in the next smaller
+    // shared-memory carve-out (more L1) at head dims 128 and 256: ~1 % at D 256.
+    float *ls_s = reinterpret_cast<float *>(sK);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S2Smem::BARS);
     uint64_t *bar_q = bars;
     uint64_t *kfull = bar_q + 1;         // [j & 1]: K_j has landed in K slot j % 2
