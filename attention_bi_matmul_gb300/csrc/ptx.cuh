@@ -54,11 +54,15 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
+// One bounded poll.  The suspend-time hint (100 us) lets the hardware park the thread
+// until the phase completes instead of returning at once, so waiting threads take
+// fewer issue slots from their neighbours (the batch sweep of linear calls: 0.817 against
+// 0.832 ms eager); the callers' time limit is checked between polls as before.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 100000;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(addr), "r"(parity)
